@@ -1,0 +1,361 @@
+"""Benchmark of the MLA speculative-verify decode on GB300.
+
+One step = one verify-decode call for each q in {1, 2, 4, 8} at H = 12 and
+ctx = 131072 with a bf16 paged cache (the q x ctx sweep of sglang PR #33650,
+"Raw q x ctx sweep" table, at its 131k column). `value` is the mean device time
+per call in microseconds; the KV bandwidth and the roofline fraction go beside it.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                        [--workload sweep131k|long_bf16|long_fp8|h96|ragged48|ragged128]
+
+Timing: each call runs as a CUDA-graph replay, bracketed by CUDA events on the
+stream it runs on; the L2 is flushed (a 256 MB write) before every timed call.
+SM clocks and throttle reasons are sampled with nvidia-smi during the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mla_speculative_verify_gb300 import inputs  # noqa: E402
+
+METRIC = "MLA verify-decode µs/call and KV GB/s as % of GB300 HBM peak, q×ctx sweep"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def workload(name: str):
+    """List of problems making up one step, and a description."""
+    if name == "sweep131k":
+        return [inputs.workload_sweep_131k(q) for q in (1, 2, 4, 8)], dict(
+            workload="h12_ctx131072_bf16_q1-2-4-8", H=12, ctx=131072, q=[1, 2, 4, 8], kv="bf16", page_size=64)
+    if name == "long_bf16":
+        return [inputs.workload_long(inputs.KV_BF16)], dict(workload="h12_q8_ctx1048576_bf16", H=12, ctx=1 << 20, q=[8],
+                                                             kv="bf16", page_size=64)
+    if name == "long_fp8":
+        return [inputs.workload_long(inputs.KV_FP8)], dict(workload="h12_q8_ctx1048576_fp8", H=12, ctx=1 << 20, q=[8],
+                                                            kv="fp8_e4m3", page_size=64)
+    if name == "h96":
+        probs = [inputs.workload_h96(q, c, kv) for q in (1, 8) for c in (32768, 131072) for kv in ("bf16", "fp8")]
+        return probs, dict(workload="h96_q1-8_ctx32768-131072_bf16-fp8", H=96, page_size=64)
+    if name.startswith("ragged"):
+        H = int(name[len("ragged"):])
+        return [inputs.workload_ragged(H, "ragged"), inputs.workload_ragged(H, "uniform")], dict(
+            workload=f"h{H}_b32_mtp3_ragged+uniform_q4_ctx16k-32k_fp8", H=H, page_size=64)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def algorithmic_bytes(prob) -> int:
+    """KV read once per request + Q + out + LSE + page table (bytes per call)."""
+    kvb = 2 if prob.kv_dtype == inputs.KV_BF16 else 1
+    H = prob.H
+    tq = prob.total_q
+    pages = int(((prob.seq_lens + 63) // 64).sum())
+    return int(prob.seq_lens.astype(np.int64).sum()) * 576 * kvb + tq * H * 576 * 2 + tq * H * 512 * 2 + tq * H * 4 + pages * 4
+
+
+def algorithmic_flops(prob) -> float:
+    f = 0.0
+    for ctx, q in zip(prob.seq_lens, prob.q_lens):
+        vis = sum(int(ctx) - int(q) + i + 1 for i in range(int(q)))
+        f += vis * prob.H * 2176.0
+    return f
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def __enter__(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_ours(args, probs, desc, rank, world):
+    from mla_speculative_verify_gb300.decoder import VerifyDecoder
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    calls = []
+    for prob in probs:
+        dec = VerifyDecoder(prob.seq_lens, prob.q_lens, prob.H, prob.kv_dtype, dev)
+        q = prob.q.to(dev)
+        kv = prob.kv.to(dev)
+        pt = torch.from_numpy(prob.page_table).to(dev)
+        out = torch.empty((prob.total_q, prob.H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((prob.total_q, prob.H), dtype=torch.float32, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        with torch.cuda.stream(stream):
+            dec.run(q, kv, pt, out, lse, prob.sm_scale, prob.kv_scale, status)  # sets attributes, warms caches
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                dec.run(q, kv, pt, out, lse, prob.sm_scale, prob.kv_scale, status)
+        calls.append(dict(prob=prob, dec=dec, q=q, kv=kv, pt=pt, out=out, lse=lse, status=status, graph=g))
+    launches_per_step = sum(1 + (1 if c["dec"].info["n_merge"] > 0 else 0) for c in calls)
+
+    def one_step(timed: bool):
+        evs = []
+        for c in calls:
+            with torch.cuda.stream(stream):
+                flush.fill_(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                c["graph"].replay()
+                e1.record(stream)
+            evs.append((e0, e1))
+        return evs
+
+    for _ in range(args.warmup):
+        one_step(False)
+    stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    all_evs = []
+    with ClockSampler(dev.index) as clk:
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            all_evs.append(one_step(True))
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    per_call_ms = np.array([[e0.elapsed_time(e1) for (e0, e1) in evs] for evs in all_evs])  # [K, calls]
+    step_ms = per_call_ms.sum(1)
+    status_bits = 0
+    for c in calls:
+        status_bits |= int(c["status"].item())
+    # end to end: host (pinned) inputs copied in and the result read back inside the timed region
+    e2e = measure_e2e(args, calls, dev, stream)
+    return dict(per_call_ms=per_call_ms, step_ms=step_ms, wall=wall, clocks=clk.summary(), status=status_bits,
+                launches=launches_per_step * args.steps, e2e=e2e, calls=calls)
+
+
+def measure_e2e(args, calls, dev, stream):
+    """Same metric through the public API with host buffers: per call the H2D copy of
+    q, the cache, the page table and the lengths, the decode, and the D2H of out and lse."""
+    hosts = []
+    for c in calls:
+        prob = c["prob"]
+        h = dict(q=prob.q.pin_memory(), kv=prob.kv.pin_memory(), pt=torch.from_numpy(prob.page_table).pin_memory(),
+                 sl=torch.from_numpy(prob.seq_lens).pin_memory(), ql=torch.from_numpy(prob.q_lens).pin_memory(),
+                 out=torch.empty(c["out"].shape, dtype=torch.bfloat16).pin_memory(),
+                 lse=torch.empty(c["lse"].shape, dtype=torch.float32).pin_memory())
+        hosts.append(h)
+    h2d = sum(h["q"].numel() * 2 + h["kv"].numel() * h["kv"].element_size() + h["pt"].numel() * 4 +
+              h["sl"].numel() * 8 for h in hosts)
+    d2h = sum(h["out"].numel() * 2 + h["lse"].numel() * 4 for h in hosts)
+    steps = max(1, min(args.steps, 5))
+
+    def step():
+        for c, h in zip(calls, hosts):
+            with torch.cuda.stream(stream):
+                c["q"].copy_(h["q"], non_blocking=True)
+                c["kv"].copy_(h["kv"], non_blocking=True)
+                c["pt"].copy_(h["pt"], non_blocking=True)
+                c["dec"].seq_lens_dev.copy_(h["sl"], non_blocking=True)
+                c["dec"].q_lens_dev.copy_(h["ql"], non_blocking=True)
+                c["dec"].run(c["q"], c["kv"], c["pt"], c["out"], c["lse"], c["prob"].sm_scale, c["prob"].kv_scale,
+                             c["status"], stream=stream)
+                h["out"].copy_(c["out"], non_blocking=True)
+                h["lse"].copy_(c["lse"], non_blocking=True)
+        stream.synchronize()
+
+    step()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return dict(ms_per_step=ms, us_per_call=ms * 1000.0 / len(calls), h2d=h2d, d2h=d2h)
+
+
+def cpu_baseline(probs, max_seconds=30.0):
+    """The float64 oracle, as it stands, on this host's cores: one call per problem of
+    the step (time-bounded: stop after max_seconds and scale by the calls done)."""
+    import oracle
+
+    oracle.build()
+    cores = os.cpu_count() or 1
+    t_total, done = 0.0, 0
+    for prob in probs:
+        kvd = oracle.KV_BF16 if prob.kv_dtype == inputs.KV_BF16 else oracle.KV_FP8_E4M3
+        bounds = [sorted(set(int(c) * i // 64 for i in range(65))) for c in prob.seq_lens]
+        t0 = time.perf_counter()
+        oracle.decode(prob.q_bits(), prob.kv_bits(), kvd, prob.kv_scale, prob.page_table, prob.page_size,
+                      prob.seq_lens, prob.q_lens, prob.H, prob.sm_scale, mode=oracle.MODE_SPLIT, split_bounds=bounds,
+                      nthreads=cores)
+        t_total += time.perf_counter() - t0
+        done += 1
+        if t_total > max_seconds:
+            break
+    return dict(us_per_call=t_total * 1e6 / done, cores=cores, calls=done,
+                sample=f"{done} of {len(probs)} calls of the step, full size, oracle split+merge mode")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="sweep131k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if args.impl == "ours" else "gloo")
+
+    probs, desc = workload(args.workload)
+    calls_per_step = len(probs)
+
+    if args.impl == "reference":
+        # the oracle is the reference arm: rank 0 only, bounded samples per step
+        if rank != 0:
+            return
+        times = []
+        for i in range(args.warmup + args.steps):
+            r = cpu_baseline(probs, max_seconds=20.0)
+            if i >= args.warmup:
+                times.append(r["us_per_call"])
+        v = statistics.median(times)
+        line = {"metric": METRIC, "value": v, "unit": "us/call", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": v * calls_per_step / 1000.0, "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {**desc, "l2": "n/a (CPU)"}, "impl": "reference",
+                "cpu_baseline": {"value": v, "unit": "us/call", "cores": r["cores"], "kind": "oracle",
+                                 "sample": r["sample"]},
+                "e2e": {"value": v, "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    res = run_ours(args, probs, desc, rank, world)
+    step_ms = float(np.median(res["step_ms"]))
+    if world > 1:
+        t = torch.tensor([step_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    us_per_call = step_ms * 1000.0 / calls_per_step
+    hbm_peak, tf_peak, peak_src = load_peaks()
+    per_call_ms = np.median(res["per_call_ms"], axis=0)
+    rows = []
+    for c, ms in zip(res["calls"], per_call_ms):
+        prob = c["prob"]
+        nbytes = algorithmic_bytes(prob)
+        flops = algorithmic_flops(prob)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rows.append(dict(name=prob.name, us=round(ms * 1000.0, 2), kv_gbs=round(gbs, 1),
+                         hbm_frac=round(gbs / hbm_peak, 3),
+                         tensor_frac=round(flops / (ms * 1e-3) / 1e12 / tf_peak, 3),
+                         units=c["dec"].info["n_units"], merge_items=c["dec"].info["n_merge"]))
+    # dominant call (largest share of the step): roofline against the measured HBM copy peak
+    dom = int(np.argmax(per_call_ms))
+    dprob = res["calls"][dom]["prob"]
+    dbytes = algorithmic_bytes(dprob)
+    achieved = dbytes / (per_call_ms[dom] * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(us_per_call, 3), "unit": "us/call", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if dprob.kv_dtype == inputs.KV_BF16 else "bf16 (fp8 e4m3 cache)",
+        "data": "synthetic",
+        "config": {**desc, "parallelism": "replicas" if world > 1 else "single", "l2": "flushed before every call",
+                   "timing": "CUDA-graph replay, CUDA events per call, median over steps", "per_call": rows},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "kernel": f"fold_decode_kernel + lse_merge_kernel ({dprob.name})",
+                     "peak_source": f"{peak_src} hbm_gbs"},
+        "clocks": res["clocks"],
+        "gpu_launches": res["launches"],
+        "e2e": {"value": round(res["e2e"]["us_per_call"], 2), "unit": "us/call",
+                "h2d_bytes_per_step": res["e2e"]["h2d"], "d2h_bytes_per_step": res["e2e"]["d2h"]},
+        "device_status": res["status"],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(probs)
+        line["cpu_baseline"] = {"value": round(cb["us_per_call"], 1), "unit": "us/call", "cores": cb["cores"],
+                                "kind": "oracle", "sample": cb["sample"]}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,789 @@
+// kernel_sm103.cu -- fused MLA speculative-verify decode for GB300 (sm_103a).
+//
+// One CTA processes one plan unit: a tile of at most kRowsCap packed query rows
+// (row = token * H + head; the q verify tokens of a fold group are folded into the
+// rows, sglang PR #33650 "Why" paragraph) against one page-aligned key range of
+// one request. The cache streams through shared memory once per unit, one 64-key
+// page per pipeline stage, and both products run on the tcgen05 tensor cores with
+// the accumulators in tensor memory, in the transposed orientation:
+//
+//   S^T[key, row]  = K[key, 0:576] . Q[row, 0:576]^T    (M = 64 keys, N = rows, K = 576)
+//   O^T[dv, row]  += V^T[dv, key] . P^T[key, row]        (M = 128 dv x 4 blocks, N = rows, K = 64 keys)
+//
+// so the MMA N dimension is exactly the packed-row count (rounded up to 16) and no
+// MMA work is spent on padding rows up to 64 or 128. V^T is the same shared-memory
+// page as K, read MN-major (the latent cache rows hold V in columns 0..511; flashinfer
+// PR #5602 "What r52 changes": the latent K stages are held until PV).
+//
+// Warp roles (one CTA per SM, 1 KV page in flight while the other is consumed):
+//   warp 0     TMA producer: Q tile once, then one page per stage (9 boxes of 64x64)
+//   warp 1     TMEM owner and MMA issuer (one elected thread)
+//   warps 2-5  softmax: each thread owns one key of the S^T tile (a TMEM lane); online
+//              softmax with a lazy per-row reference: the reference moves (and O is
+//              rescaled in TMEM) only when a score exceeds it by kRefSlack octaves
+//              (the conditional-rescale idea of flashinfer PR #5602, deferred O rescale);
+//              then the epilogue: O / l to bf16 out and LSE, or fp32 partials
+//   warps 6-9  (fp8 cache only) convert the e4m3 page to bf16 in place (exact), the
+//              per-tensor scale folded into the score scale and the output scale
+//
+// Every mbarrier wait is bounded; on expiry the kernel ORs MLA_DEVICE_WAIT_TIMEOUT into
+// the status word, stops the unit, drains its in-flight copies and frees its TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "mla_decode.h"
+#include "plan_format.h"
+#include "ptx.cuh"
+#include "status.h"
+
+namespace mla {
+
+// ------------------------------------------------------------------ tile geometry
+constexpr int kRowsCap = 48;                       // packed rows per CTA (shared-memory bound)
+constexpr int kTileKeys = 64;                      // keys per stage = one page
+constexpr int kChunks = 9;                         // 576 = 9 x 64 columns (128-byte swizzle rows)
+constexpr int kQChunkBytes = kRowsCap * 128;       // 6144
+constexpr int kQBytes = kChunks * kQChunkBytes;    // 55296
+constexpr int kKvChunkBytes = kTileKeys * 128;     // 8192
+constexpr int kSlotBytes = kChunks * kKvChunkBytes;  // 73728 (bf16 page)
+constexpr int kFp8StageOff = kSlotBytes / 2;       // e4m3 page lands in the upper half of its slot
+constexpr int kFp8ChunkBytes = kTileKeys * 64;     // 4096
+constexpr int kPtBytes = kTileKeys * 128;          // P^T tile: 64 keys x (<= 64 rows) bf16
+constexpr int kOffQ = 0;
+constexpr int kOffKv = kOffQ + kQBytes;
+constexpr int kOffPt = kOffKv + 2 * kSlotBytes;
+constexpr int kOffMisc = kOffPt + 2 * kPtBytes;
+constexpr int kMiscBytes = 4096;
+constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory");
+static_assert(kOffKv % 1024 == 0 && kOffPt % 1024 == 0 && kOffMisc % 1024 == 0, "1024-byte swizzle atoms");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 0;       // O^T block b at columns 64 b (N <= 64)
+constexpr uint32_t kTmemS = 256;     // S^T buffer i at columns 256 + 64 i
+constexpr float kRefSlack = 8.0f;    // octaves a score may exceed the row reference before it moves
+constexpr long long kWaitBudget = 2000000000LL;  // cycles (~1 s) before a wait gives up
+
+// Rows of an M = 64 accumulator occupy TMEM lanes 16 per 32-lane quadrant:
+// row r -> lane 32 * (r / 16) + r % 16.
+__device__ __forceinline__ int m64_row_of_lane(int quadrant, int lane) { return lane < 16 ? quadrant * 16 + lane : -1; }
+
+struct Params {
+  const uint8_t* plan;
+  const int32_t* page_table;
+  int pt_stride, num_pages, H;
+  const int32_t* seq_lens;
+  const int32_t* q_lens;
+  float score_scale_log2;  // sm_scale * kv_scale * log2(e)
+  float out_scale;         // kv_scale (1 for a bf16 cache)
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  int32_t* status;
+};
+
+struct Misc {
+  uint64_t bar_q;
+  uint64_t kv_full[2], kv_ready[2], kv_empty[2];
+  uint64_t s_full[2], s_empty[2], p_full[2], pt_empty[2];
+  uint64_t mma_done;
+  uint64_t grp_softmax, grp_dequant;  // bounded barriers among the 4 warps of a group
+  uint32_t tmem_base;
+  int abort;
+  int unit[8];
+  int req[4];
+  int flags[2][4];
+  float ref[64];
+  float alpha[64];
+  int lim[64];
+  float colred[4][64];
+  float lsum[64];
+};
+static_assert(sizeof(Misc) <= kMiscBytes, "misc block too small");
+
+__device__ __forceinline__ void report(int32_t* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// Bounded wait: false when the budget ran out or another warp aborted the unit.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitBudget) {
+      *abort = 1;
+      report(status, MLA_DEVICE_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the result is broadcast to the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort, status) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Barrier among the four warps of a group, built on an mbarrier (count 4) so that it
+// is bounded like every other wait: a warp that gave up never leaves the others stuck.
+__device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, volatile int* abort, int32_t* status) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar);
+  const bool ok = warp_wait(bar, phase & 1, abort, status);
+  ++phase;
+  return ok;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// e4m3 x4 (one 32-bit word) -> bf16 x4 (two 32-bit words), exact.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
+  __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+  float2 f0 = __half22float2(*reinterpret_cast<__half2*>(&h0));
+  float2 f1 = __half22float2(*reinterpret_cast<__half2*>(&h1));
+  lo = pack_bf16(f0.x, f0.y);
+  hi = pack_bf16(f1.x, f1.y);
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
+    fold_decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv, Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  Misc* ms = (Misc*)(smem + kOffMisc);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int* abort = &ms->abort;
+
+  ptx::pdl_launch_dependents();
+
+  const PlanHeader* ph = (const PlanHeader*)p.plan;
+  if (tid == 0) {
+    const PlanUnit* u = (const PlanUnit*)(p.plan + ph->units_off) + blockIdx.x;
+    const PlanRequest* r = (const PlanRequest*)(p.plan + ph->req_off) + u->b;
+    ms->unit[0] = u->b; ms->unit[1] = u->qrow0; ms->unit[2] = u->nrows; ms->unit[3] = u->kv_begin;
+    ms->unit[4] = u->kv_end; ms->unit[5] = u->part_row0;
+    ms->req[0] = r->ctx; ms->req[1] = r->q; ms->req[2] = r->tok0;
+    int bad = (p.seq_lens[u->b] != r->ctx || p.q_lens[u->b] != r->q) ? 1 : 0;
+    if (bad) report(p.status, MLA_DEVICE_PLAN_MISMATCH);
+    ms->abort = bad;
+    ptx::mbar_init(&ms->bar_q, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&ms->kv_full[i], 1);
+      ptx::mbar_init(&ms->kv_ready[i], 4);
+      ptx::mbar_init(&ms->kv_empty[i], 1);
+      ptx::mbar_init(&ms->s_full[i], 1);
+      ptx::mbar_init(&ms->s_empty[i], 4);
+      ptx::mbar_init(&ms->p_full[i], 4);
+      ptx::mbar_init(&ms->pt_empty[i], 1);
+    }
+    ptx::mbar_init(&ms->mma_done, 1);
+    ptx::mbar_init(&ms->grp_softmax, 4);
+    ptx::mbar_init(&ms->grp_dequant, 4);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&ms->tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+
+  const int b = ms->unit[0], qrow0 = ms->unit[1], nrows = ms->unit[2];
+  const int kv_begin = ms->unit[3], kv_end = ms->unit[4], part_row0 = ms->unit[5];
+  const int ctx = ms->req[0], qlen = ms->req[1], tok0 = ms->req[2];
+  const int ntiles = (kv_end - kv_begin + kTileKeys - 1) / kTileKeys;
+  const int nmma = (nrows + 15) & ~15;   // MMA N (rows rounded up to 16)
+  const int nch = nmma / 16;             // 16-column chunks of S^T / O^T
+  const uint32_t tmem = ms->tmem_base;
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sKv = smem + kOffKv;
+  uint8_t* sPt = smem + kOffPt;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int issued = 0;
+    bool q_issued = false;
+    if (!*abort) {
+      q_issued = true;
+      if (lane == 0) {
+        ptx::prefetch_tmap(&tmap_q);
+        ptx::prefetch_tmap(&tmap_kv);
+        const int nbox = nmma / 16;
+        ptx::mbar_arrive_expect_tx(&ms->bar_q, kChunks * nbox * 16 * 128);
+        for (int c = 0; c < kChunks; ++c)
+          for (int r = 0; r < nbox; ++r)
+            ptx::tma_load_2d(sQ + c * kQChunkBytes + r * 2048, &tmap_q, &ms->bar_q, 64 * c, qrow0 + 16 * r);
+      }
+      const int32_t* pt_row = p.page_table + (size_t)b * p.pt_stride + kv_begin / kPage;
+      for (int t0 = 0; t0 < ntiles && !*abort; t0 += 32) {
+        int pid = 0;
+        if (t0 + lane < ntiles) {
+          pid = pt_row[t0 + lane];
+          if (pid < 0 || pid >= p.num_pages) {
+            report(p.status, MLA_DEVICE_BAD_PAGE);
+            pid = 0;
+          }
+        }
+        const int cnt = min(32, ntiles - t0);
+        for (int i = 0; i < cnt; ++i) {
+          const int page = __shfl_sync(0xffffffffu, pid, i);
+          const int t = t0 + i, slot = t & 1;
+          int ok = 1;
+          if (lane == 0) {
+            if (t >= 2) ok = wait_bar(&ms->kv_empty[slot], ((t - 2) >> 1) & 1, abort, p.status);
+            if (ok) {
+              uint8_t* dst = sKv + slot * kSlotBytes;
+              if (kFp8) {
+                ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], kChunks * kFp8ChunkBytes);
+                for (int c = 0; c < kChunks; ++c)
+                  ptx::tma_load_2d(dst + kFp8StageOff + c * kFp8ChunkBytes, &tmap_kv, &ms->kv_full[slot], 64 * c,
+                                   page * kPage);
+              } else {
+                ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], kChunks * kKvChunkBytes);
+                for (int c = 0; c < kChunks; ++c)
+                  ptx::tma_load_2d(dst + c * kKvChunkBytes, &tmap_kv, &ms->kv_full[slot], 64 * c, page * kPage);
+              }
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          issued = t + 1;
+        }
+      }
+    }
+    // Drain: every issued copy must have landed before the CTA may exit (at most the
+    // last two pages can still be in flight; earlier ones were consumed by the MMAs).
+    if (lane == 0) {
+      for (int t = max(0, issued - 2); t < issued; ++t) {
+        long long t0c = clock64();
+        while (!ptx::mbar_try_wait(&ms->kv_full[t & 1], (t >> 1) & 1) && clock64() - t0c < kWaitBudget) {
+        }
+      }
+      if (q_issued) {
+        long long t0c = clock64();
+        while (!ptx::mbar_try_wait(&ms->bar_q, 0) && clock64() - t0c < kWaitBudget) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && !*abort) {
+      const uint32_t sq = ptx::smem_addr(sQ), skv = ptx::smem_addr(sKv), spt = ptx::smem_addr(sPt);
+      const uint32_t idesc_s = ptx::idesc_bf16(64, nmma, 0, 0);    // S^T: K-major K tile, K-major Q
+      const uint32_t idesc_o = ptx::idesc_bf16(128, nmma, 1, 1);   // O^T: MN-major V^T, MN-major P^T
+      bool ok = wait_bar(&ms->bar_q, 0, abort, p.status);
+      for (int t = 0; ok && t <= ntiles; ++t) {
+        if (t < ntiles) {
+          const int slot = t & 1;
+          ok = wait_bar(kFp8 ? &ms->kv_ready[slot] : &ms->kv_full[slot], (t >> 1) & 1, abort, p.status);
+          if (ok && t >= 2) ok = wait_bar(&ms->s_empty[slot], ((t - 2) >> 1) & 1, abort, p.status);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint32_t a0 = skv + slot * kSlotBytes;
+          const uint32_t d = tmem + kTmemS + 64 * slot;
+#pragma unroll 1
+          for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint64_t ad = ptx::smem_desc(a0 + c * kKvChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
+              uint64_t bd = ptx::smem_desc(sq + c * kQChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
+              ptx::mma_bf16_ss(d, ad, bd, idesc_s, (c | k) != 0);
+            }
+          }
+          ptx::mma_commit(&ms->s_full[slot]);
+        }
+        if (t >= 1) {
+          const int u = t - 1, ub = u & 1;
+          ok = wait_bar(&ms->p_full[ub], (u >> 1) & 1, abort, p.status);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint32_t v0 = skv + ub * kSlotBytes, pt0 = spt + ub * kPtBytes;
+#pragma unroll 1
+          for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint64_t ad = ptx::smem_desc(v0 + 2 * blk * kKvChunkBytes + 2048 * k, kKvChunkBytes, 1024, ptx::kSwizzle128B);
+              uint64_t bd = ptx::smem_desc(pt0 + 2048 * k, 8192, 1024, ptx::kSwizzle128B);
+              ptx::mma_bf16_ss(tmem + kTmemO + 64 * blk, ad, bd, idesc_o, (u > 0 || k > 0) ? 1u : 0u);
+            }
+          }
+          ptx::mma_commit(&ms->kv_empty[ub]);
+          ptx::mma_commit(&ms->pt_empty[ub]);
+        }
+      }
+      // all issued MMAs must retire before TMEM is released
+      ptx::mma_commit(&ms->mma_done);
+      long long t0c = clock64();
+      while (!ptx::mbar_try_wait(&ms->mma_done, 0) && clock64() - t0c < kWaitBudget) {
+      }
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int qd = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int sidx = tid - 64;               // 0..127
+    const int krow = m64_row_of_lane(qd, lane);
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    uint32_t gphase = 0;
+    if (sidx < 64) {
+      int lim = 0;
+      if (sidx < nrows) {
+        const int i = (qrow0 + sidx) / p.H - tok0;  // verify token of this packed row
+        lim = ctx - qlen + i + 1;
+      }
+      ms->lim[sidx] = lim;
+      ms->ref[sidx] = -INFINITY;
+    }
+    bool ok = group_sync(&ms->grp_softmax, gphase, abort, p.status) && !*abort;
+    float l_acc[kRowsCap];
+#pragma unroll
+    for (int n = 0; n < kRowsCap; ++n) l_acc[n] = 0.f;
+    for (int t = 0; ok && t < ntiles; ++t) {
+      const int sb = t & 1;
+      ok = warp_wait(&ms->s_full[sb], (t >> 1) & 1, abort, p.status);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      float x[kRowsCap];
+#pragma unroll
+      for (int c = 0; c < kRowsCap / 16; ++c)
+        if (c < nch) ptx::tmem_ld16(tmem + kTmemS + 64 * sb + lane_off + 16 * c, x + 16 * c);
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ms->s_empty[sb]);
+      const int key = kv_begin + t * kTileKeys + krow;
+      const bool valid = krow >= 0 && key < kv_end;
+      bool need = false;
+#pragma unroll
+      for (int n = 0; n < kRowsCap; ++n) {
+        if (n < nmma) {
+          const float v = (valid && key < ms->lim[n]) ? x[n] * p.score_scale_log2 : -INFINITY;
+          x[n] = v;
+          need |= v > ms->ref[n] + kRefSlack;
+        }
+      }
+      const unsigned vote = __any_sync(0xffffffffu, need);
+      if (lane == 0) ms->flags[sb][qd] = vote ? 1 : 0;
+      ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
+      if (!ok) break;
+      const bool moved = ms->flags[sb][0] | ms->flags[sb][1] | ms->flags[sb][2] | ms->flags[sb][3];
+      if (moved) {
+        // column maxima over this tile's keys, then move each row's reference up to it
+#pragma unroll
+        for (int n = 0; n < kRowsCap; ++n) {
+          if (n < nmma) {
+            float m = x[n];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) ms->colred[qd][n] = m;
+          }
+        }
+        ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
+        if (!ok) break;
+        if (sidx < nmma) {
+          const float cm = fmaxf(fmaxf(ms->colred[0][sidx], ms->colred[1][sidx]), fmaxf(ms->colred[2][sidx], ms->colred[3][sidx]));
+          const float old = ms->ref[sidx];
+          const float nw = fmaxf(old, cm);
+          ms->alpha[sidx] = (nw == old) ? 1.f : ex2(old - nw);
+          ms->ref[sidx] = nw;
+        }
+        ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
+        if (!ok) break;
+#pragma unroll
+        for (int n = 0; n < kRowsCap; ++n)
+          if (n < nmma) l_acc[n] *= ms->alpha[n];
+        if (t >= 1) {
+          // O^T holds tiles < t: wait for PV(t-1), then scale each row's column by alpha
+          ok = warp_wait(&ms->pt_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, p.status);
+          if (!ok) break;
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll 1
+            for (int c = 0; c < nch; ++c) {
+              float o[16];
+              const uint32_t ta = tmem + kTmemO + 64 * blk + lane_off + 16 * c;
+              ptx::tmem_ld16(ta, o);
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) o[j] *= ms->alpha[16 * c + j];
+              ptx::tmem_st16(ta, o);
+            }
+          }
+          ptx::tmem_st_wait();
+        }
+      }
+      // probabilities relative to the (possibly moved) reference
+      uint32_t pk[kRowsCap / 2];
+#pragma unroll
+      for (int n = 0; n < kRowsCap; n += 2) {
+        float p0 = 0.f, p1 = 0.f;
+        if (n < nmma) {
+          p0 = x[n] == -INFINITY ? 0.f : ex2(x[n] - ms->ref[n]);
+          p1 = x[n + 1] == -INFINITY ? 0.f : ex2(x[n + 1] - ms->ref[n + 1]);
+          l_acc[n] += p0;
+          l_acc[n + 1] += p1;
+        }
+        pk[n / 2] = pack_bf16(p0, p1);
+      }
+      if (t >= 2) {
+        ok = warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p.status);
+        if (!ok) break;
+      }
+      if (krow >= 0) {
+        uint8_t* line = sPt + sb * kPtBytes + krow * 128;
+#pragma unroll
+        for (int j = 0; j < kRowsCap / 8; ++j)
+          if (j < nmma / 8)
+            *reinterpret_cast<uint4*>(line + (((j ^ (krow & 7)) & 7) << 4)) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        if (key >= kv_end) {
+          // a cache slot past the key range: zero its value columns so P = 0 meets V = 0
+          uint8_t* slot = sKv + sb * kSlotBytes + krow * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(slot + c * kKvChunkBytes + 16 * j) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      ptx::fence_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ms->p_full[sb]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok) ok = warp_wait(&ms->pt_empty[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort, p.status);
+    if (ok) {
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int n = 0; n < kRowsCap; ++n) {
+        if (n < nmma) {
+          float s = l_acc[n];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+          if (lane == 0) ms->colred[qd][n] = s;
+        }
+      }
+      ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
+    }
+    if (ok) {
+      if (sidx < nrows) {
+        const float L = ms->colred[0][sidx] + ms->colred[1][sidx] + ms->colred[2][sidx] + ms->colred[3][sidx];
+        ms->lsum[sidx] = L;
+        const float lse_v = L > 0.f ? (ms->ref[sidx] + lg2(L)) * 0.69314718055994531f : -INFINITY;
+        if (part_row0 < 0) {
+          if (p.lse) p.lse[qrow0 + sidx] = lse_v;
+        } else {
+          p.part_lse[part_row0 + sidx] = lse_v;
+        }
+      }
+      ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
+    }
+    if (ok) {
+      const int dv_in_blk = qd * 32 + lane;
+#pragma unroll 1
+      for (int blk = 0; blk < 4; ++blk) {
+        const int dv = blk * 128 + dv_in_blk;
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+          float o[16];
+          ptx::tmem_ld16(tmem + kTmemO + 64 * blk + lane_off + 16 * c, o);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int n = 16 * c + j;
+            if (n < nrows) {
+              const float L = ms->lsum[n];
+              const float v = L > 0.f ? o[j] * (p.out_scale / L) : 0.f;
+              if (part_row0 < 0)
+                p.out[(size_t)(qrow0 + n) * kDv + dv] = __float2bfloat16_rn(v);
+              else
+                p.part_o[(size_t)(part_row0 + n) * kDv + dv] = v;
+            }
+          }
+        }
+      }
+    }
+  } else if (kFp8) {
+    // ------------------------------------------------------------ e4m3 -> bf16 (in place)
+    const int didx = tid - 192;        // 0..127
+    const int k = didx >> 1, half = didx & 1;
+    uint32_t gphase = 0;
+    bool ok = !*abort;
+    for (int t = 0; ok && t < ntiles; ++t) {
+      const int slot = t & 1;
+      ok = warp_wait(&ms->kv_full[slot], (t >> 1) & 1, abort, p.status);
+      if (!ok) break;
+      uint8_t* base = sKv + slot * kSlotBytes;
+      uint4 raw[kChunks][2];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const uint8_t* src = base + kFp8StageOff + c * kFp8ChunkBytes + k * 64 + half * 32;
+        raw[c][0] = *reinterpret_cast<const uint4*>(src);
+        raw[c][1] = *reinterpret_cast<const uint4*>(src + 16);
+      }
+      // every e4m3 byte of the page is read before any bf16 byte is written over it
+      ok = group_sync(&ms->grp_dequant, gphase, abort, p.status);
+      if (!ok) break;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        uint8_t* line = base + c * kKvChunkBytes + k * 128;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 w = raw[c][h];
+          uint4 o0, o1;
+          e4m3x4_to_bf16x4(w.x, o0.x, o0.y);
+          e4m3x4_to_bf16x4(w.y, o0.z, o0.w);
+          e4m3x4_to_bf16x4(w.z, o1.x, o1.y);
+          e4m3x4_to_bf16x4(w.w, o1.z, o1.w);
+          const int j0 = half * 4 + h * 2;  // 16-byte chunk index within the 128-byte row
+          *reinterpret_cast<uint4*>(line + (((j0) ^ (k & 7)) << 4)) = o0;
+          *reinterpret_cast<uint4*>(line + (((j0 + 1) ^ (k & 7)) << 4)) = o1;
+        }
+      }
+      ptx::fence_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ms->kv_ready[slot]);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ LSE merge
+// One warp per packed row: L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s
+// (a split a causal row cannot see has L_s = -inf and is skipped).
+__global__ void __launch_bounds__(128) lse_merge_kernel(const uint8_t* plan, const float* part_o, const float* part_lse,
+                                                       __nv_bfloat16* out, float* lse) {
+  ptx::pdl_wait_primary();
+  const PlanHeader* ph = (const PlanHeader*)plan;
+  const PlanMerge m = ((const PlanMerge*)(plan + ph->merge_off))[blockIdx.y];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + warp;
+  if (row >= m.nrows) return;
+  const int ns = m.n_splits;
+  float mx = -INFINITY;
+  for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, part_lse[m.part_row0 + s * m.nrows + row]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float sum = 0.f;
+  for (int s = lane; s < ns; s += 32) {
+    const float v = part_lse[m.part_row0 + s * m.nrows + row];
+    if (v != -INFINITY) sum += __expf(v - mx);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float L = mx + __logf(sum);
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < ns; ++s) {
+    const int pr = m.part_row0 + s * m.nrows + row;
+    const float v = part_lse[pr];
+    if (v == -INFINITY) continue;
+    const float w = __expf(v - L);
+    const float4* src = reinterpret_cast<const float4*>(part_o + (size_t)pr * kDv);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 x = src[j * 32 + lane];
+      acc[j].x += w * x.x; acc[j].y += w * x.y; acc[j].z += w * x.z; acc[j].w += w * x.w;
+    }
+  }
+  const int qr = m.qrow0 + row;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint2 pk = make_uint2(pack_bf16(acc[j].x, acc[j].y), pack_bf16(acc[j].z, acc[j].w));
+    *reinterpret_cast<uint2*>(out + (size_t)qr * kDv + 4 * (j * 32 + lane)) = pk;
+  }
+  if (lse && lane == 0) lse[qr] = L;
+}
+
+int rows_cap_for(int kv_dtype) {
+  (void)kv_dtype;
+  return kRowsCap;
+}
+
+// ------------------------------------------------------------------ host side
+size_t workspace_bytes_for(int n_part_rows);
+int check_plan(const void* plan_host, size_t plan_bytes, const PlanHeader** out);
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  bool checked = false, ok = false, attrs_set = false;
+  int major = 0, minor = 0;
+};
+static DeviceInfo g_dev[64];
+static std::mutex g_dev_mu;
+
+static int prepare_device(int dev) {
+  if (dev < 0 || dev >= 64) return set_error(MLA_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.checked) {
+    cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    d.ok = (d.major == 10 && d.minor == 3);
+    d.checked = true;
+  }
+  if (!d.ok)
+    return set_error(MLA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a (GB300)", dev, d.major,
+                     d.minor);
+  if (!d.attrs_set) {
+    cudaError_t e1 = cudaFuncSetAttribute(fold_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e2 = cudaFuncSetAttribute(fold_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e1 != cudaSuccess || e2 != cudaSuccess)
+      return set_error(MLA_ERR_CUDA, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e1 != cudaSuccess ? e1 : e2));
+    d.attrs_set = true;
+  }
+  return MLA_OK;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_t plan_bytes, const void* q,
+                              const void* kv_cache, const int32_t* page_table, int page_table_stride, int num_pages,
+                              const int32_t* seq_lens, const int32_t* q_lens, float sm_scale, float kv_scale, void* out,
+                              float* lse, void* workspace, size_t workspace_bytes, int32_t* status_dev, void* stream) {
+  clear_error();
+  const PlanHeader* h = nullptr;
+  int rc = check_plan(plan_host, plan_bytes, &h);
+  if (rc != MLA_OK) return rc;
+  if (!plan_dev || !q || !kv_cache || !page_table || !seq_lens || !q_lens || !out)
+    return set_error(MLA_ERR_INVALID_ARG, "plan_dev, q, kv_cache, page_table, seq_lens, q_lens and out must not be NULL");
+  if (!aligned16(plan_dev) || !aligned16(q) || !aligned16(kv_cache) || !aligned16(out))
+    return set_error(MLA_ERR_INVALID_ARG, "plan_dev, q, kv_cache and out must be 16-byte aligned");
+  if (((uintptr_t)page_table & 3u) || ((uintptr_t)seq_lens & 3u) || ((uintptr_t)q_lens & 3u) || ((uintptr_t)lse & 3u) ||
+      ((uintptr_t)status_dev & 3u))
+    return set_error(MLA_ERR_INVALID_ARG, "page_table, seq_lens, q_lens, lse and status_dev must be 4-byte aligned");
+  if (num_pages < 1) return set_error(MLA_ERR_INVALID_ARG, "num_pages must be >= 1 (got %d)", num_pages);
+  if (page_table_stride < h->max_pages)
+    return set_error(MLA_ERR_INVALID_ARG, "page_table_stride %d is smaller than the %d pages of the longest request",
+                     page_table_stride, h->max_pages);
+  if (!(sm_scale > 0.f) || !(kv_scale > 0.f) || !isfinite(sm_scale) || !isfinite(kv_scale))
+    return set_error(MLA_ERR_INVALID_ARG, "sm_scale and kv_scale must be finite and > 0");
+  const size_t ws_need = workspace_bytes_for(h->n_part_rows);
+  if (ws_need > 0 && (!workspace || workspace_bytes < ws_need))
+    return set_error(MLA_ERR_BUFFER, "workspace needs %zu bytes (got %zu)", ws_need, workspace ? workspace_bytes : (size_t)0);
+  if (ws_need > 0 && ((uintptr_t)workspace & 255u)) return set_error(MLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if ((long long)num_pages * kPage > 0xFFFFFFFFLL) return set_error(MLA_ERR_INVALID_ARG, "num_pages too large");
+  if (h->n_units == 0) return MLA_OK;
+
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
+  rc = prepare_device(dev);
+  if (rc != MLA_OK) return rc;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encoder();
+  if (!enc) return set_error(MLA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+
+  alignas(64) CUtensorMap tq, tkv;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kDqk, (cuuint64_t)h->total_q * (cuuint64_t)h->num_heads};
+    cuuint64_t strides[1] = {(cuuint64_t)kDqk * 2};
+    cuuint32_t box[2] = {64, 16};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(MLA_ERR_CUDA, "tensor map for q failed (CUresult %d)", (int)r);
+  }
+  const bool fp8 = h->kv_dtype == MLA_KV_FP8_E4M3;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kDqk, (cuuint64_t)num_pages * kPage};
+    cuuint64_t strides[1] = {(cuuint64_t)kDqk * (fp8 ? 1 : 2)};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(&tkv, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<void*>(kv_cache), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(MLA_ERR_CUDA, "tensor map for kv_cache failed (CUresult %d)", (int)r);
+  }
+
+  Params prm;
+  prm.plan = (const uint8_t*)plan_dev;
+  prm.page_table = page_table;
+  prm.pt_stride = page_table_stride;
+  prm.num_pages = num_pages;
+  prm.H = h->num_heads;
+  prm.seq_lens = seq_lens;
+  prm.q_lens = q_lens;
+  const float ks = fp8 ? kv_scale : 1.0f;
+  prm.score_scale_log2 = sm_scale * ks * 1.4426950408889634f;
+  prm.out_scale = ks;
+  prm.out = (__nv_bfloat16*)out;
+  prm.lse = lse;
+  prm.part_o = (float*)workspace;
+  prm.part_lse = ws_need ? (float*)((uint8_t*)workspace + ((size_t)h->n_part_rows * kDv * sizeof(float) + 255) / 256 * 256)
+                         : nullptr;
+  prm.status = status_dev;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (fp8)
+    fold_decode_kernel<true><<<h->n_units, 320, kSmemBytes, st>>>(tq, tkv, prm);
+  else
+    fold_decode_kernel<false><<<h->n_units, 192, kSmemBytes, st>>>(tq, tkv, prm);
+  ce = cudaGetLastError();
+  if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "fold kernel launch: %s", cudaGetErrorString(ce));
+  if (h->n_merge > 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((h->rows_cap + 3) / 4), (unsigned)h->n_merge, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    ce = cudaLaunchKernelEx(&cfg, lse_merge_kernel, (const uint8_t*)plan_dev, (const float*)prm.part_o,
+                            (const float*)prm.part_lse, (__nv_bfloat16*)out, lse);
+    if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "merge kernel launch: %s", cudaGetErrorString(ce));
+  }
+  return MLA_OK;
+}

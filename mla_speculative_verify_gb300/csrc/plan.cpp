@@ -1,0 +1,215 @@
+// plan.cpp -- host-only split-KV work partition for MLA verify decode.
+//
+// The planner works from host-known scalars only (seq_lens, q_lens, H, the SM
+// count), as the host plan of flashinfer PR #5588 ("What was measured" table,
+// host-plan row) does. Steps:
+//   1. fold_sq (sglang PR #33650, "Why" paragraph): F = largest divisor of q with
+//      H * F <= 128; the q tokens form q / F groups of F * H packed rows
+//      (row = token * H + head, contiguous in Q and in the output).
+//   2. A group's packed rows are cut into CTA row tiles of at most rows_cap rows
+//      (the shared-memory budget of one CTA, see kernel_sm103.cu). The tiles of
+//      one group are adjacent in the unit list, so they stream the same pages at
+//      the same time and the second read is served by L2.
+//   3. Each row tile's key range [0, ctx) is cut into page-aligned splits so that
+//      the units fill the SMs; split units write partial (O, LSE) rows that the
+//      merge kernel combines.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "mla_decode.h"
+#include "plan_format.h"
+#include "status.h"
+
+namespace mla {
+
+int rows_cap_for(int kv_dtype);  // defined next to the kernel
+
+static int fold_factor(int q, int H) {
+  int best = 1;
+  for (int f = 1; f <= q; ++f)
+    if (q % f == 0 && (long long)H * f <= 128) best = f;
+  return best;
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t workspace_bytes_for(int n_part_rows) {
+  if (n_part_rows <= 0) return 0;
+  return align_up((size_t)n_part_rows * kDv * sizeof(float), 256) + align_up((size_t)n_part_rows * sizeof(float), 256);
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_lens_h, int batch, int num_heads,
+                                  int page_size, int kv_dtype, int num_sms, const mla_plan_options* opts,
+                                  void* plan_buf, size_t plan_buf_bytes, size_t* plan_bytes_out,
+                                  size_t* workspace_bytes_out) {
+  clear_error();
+  if (!seq_lens_h || !q_lens_h) return set_error(MLA_ERR_INVALID_ARG, "seq_lens_h and q_lens_h must not be NULL");
+  if (batch < 1) return set_error(MLA_ERR_INVALID_ARG, "batch must be >= 1 (got %d)", batch);
+  if (num_heads < 1 || num_heads > MLA_MAX_HEADS)
+    return set_error(MLA_ERR_UNSUPPORTED, "num_heads must be in [1, %d] (got %d)", MLA_MAX_HEADS, num_heads);
+  if (page_size != kPage) return set_error(MLA_ERR_UNSUPPORTED, "only page_size 64 is supported (got %d)", page_size);
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3)
+    return set_error(MLA_ERR_INVALID_ARG, "kv_dtype must be MLA_KV_BF16 or MLA_KV_FP8_E4M3 (got %d)", kv_dtype);
+  if (num_sms < 1) return set_error(MLA_ERR_INVALID_ARG, "num_sms must be >= 1 (got %d)", num_sms);
+  mla_plan_options o{};
+  if (opts) o = *opts;
+  int cap = rows_cap_for(kv_dtype);
+  if (o.max_rows_per_cta > 0) {
+    if (o.max_rows_per_cta % 16 != 0 || o.max_rows_per_cta > cap)
+      return set_error(MLA_ERR_INVALID_ARG, "max_rows_per_cta must be a multiple of 16 and <= %d (got %d)", cap,
+                       o.max_rows_per_cta);
+    cap = o.max_rows_per_cta;
+  }
+  if (o.force_splits < 0 || o.min_pages_per_split < 0 || o.force_fold < 0)
+    return set_error(MLA_ERR_INVALID_ARG, "plan options must be >= 0");
+
+  long long total_q = 0;
+  int max_pages = 0;
+  for (int b = 0; b < batch; ++b) {
+    int ctx = seq_lens_h[b], q = q_lens_h[b];
+    if (q < 1) return set_error(MLA_ERR_INVALID_ARG, "q_lens[%d] = %d must be >= 1", b, q);
+    if (ctx < q) return set_error(MLA_ERR_INVALID_ARG, "seq_lens[%d] = %d is smaller than q_lens[%d] = %d", b, ctx, b, q);
+    if (o.force_fold > 0 && q % o.force_fold != 0)
+      return set_error(MLA_ERR_INVALID_ARG, "force_fold %d does not divide q_lens[%d] = %d", o.force_fold, b, q);
+    total_q += q;
+    max_pages = std::max(max_pages, (ctx + kPage - 1) / kPage);
+  }
+  if (total_q * num_heads > (1LL << 30)) return set_error(MLA_ERR_INVALID_ARG, "too many query rows");
+
+  // --- row tiles ----------------------------------------------------------------------
+  struct RowTile { int b, qrow0, nrows, pages; };
+  std::vector<RowTile> tiles;
+  std::vector<PlanRequest> reqs(batch);
+  long long total_page_work = 0;
+  int tok0 = 0;
+  for (int b = 0; b < batch; ++b) {
+    int ctx = seq_lens_h[b], q = q_lens_h[b];
+    int F = o.force_fold > 0 ? o.force_fold : fold_factor(q, num_heads);
+    reqs[b] = PlanRequest{ctx, q, tok0, F};
+    int R = F * num_heads;                       // packed rows per fold group
+    int n_rt = (R + cap - 1) / cap;
+    int T = ((R + n_rt - 1) / n_rt + 15) / 16 * 16;
+    if (T > cap) T = cap;
+    int pages = (ctx + kPage - 1) / kPage;
+    for (int g = 0; g < q / F; ++g) {
+      int grow0 = (tok0 + g * F) * num_heads;
+      for (int r0 = 0; r0 < R; r0 += T) {
+        tiles.push_back(RowTile{b, grow0 + r0, std::min(T, R - r0), pages});
+        total_page_work += pages;
+      }
+    }
+    tok0 += q;
+  }
+
+  // --- splits ----------------------------------------------------------------------
+  int min_pages = o.min_pages_per_split > 0 ? o.min_pages_per_split : 4;
+  long long target_units = num_sms;
+  long long per_unit = std::max<long long>(min_pages, (total_page_work + target_units - 1) / target_units);
+  std::vector<PlanUnit> units;
+  std::vector<PlanMerge> merges;
+  int part_rows = 0;
+  // group the row tiles of one fold group so that equal splits are adjacent
+  size_t i = 0;
+  while (i < tiles.size()) {
+    size_t j = i;  // tiles [i, j) share (b, group): consecutive with equal b and pages, qrow0 contiguous
+    int grp_rows = 0;
+    const int b = tiles[i].b;
+    const int R = reqs[b].fold * num_heads;
+    while (j < tiles.size() && tiles[j].b == b && grp_rows < R) { grp_rows += tiles[j].nrows; ++j; }
+    int pages = tiles[i].pages;
+    int n_split = o.force_splits > 0 ? o.force_splits : (int)((pages + per_unit - 1) / per_unit);
+    n_split = std::max(1, std::min(n_split, pages));
+    std::vector<int> part0(j - i, -1);
+    if (n_split > 1) {
+      for (size_t t = i; t < j; ++t) {
+        part0[t - i] = part_rows;
+        merges.push_back(PlanMerge{tiles[t].qrow0, tiles[t].nrows, part_rows, n_split});
+        part_rows += n_split * tiles[t].nrows;
+      }
+    }
+    for (int s = 0; s < n_split; ++s) {
+      int p_begin = (int)((long long)pages * s / n_split), p_end = (int)((long long)pages * (s + 1) / n_split);
+      int kb = p_begin * kPage, ke = std::min(reqs[b].ctx, p_end * kPage);
+      for (size_t t = i; t < j; ++t) {
+        PlanUnit u;
+        u.b = b; u.qrow0 = tiles[t].qrow0; u.nrows = tiles[t].nrows;
+        u.kv_begin = kb; u.kv_end = ke;
+        u.part_row0 = n_split > 1 ? part0[t - i] + s * tiles[t].nrows : -1;
+        u.split = s; u.n_splits = n_split;
+        units.push_back(u);
+      }
+    }
+    i = j;
+  }
+
+  size_t req_off = sizeof(PlanHeader);
+  size_t units_off = align_up(req_off + sizeof(PlanRequest) * batch, 32);
+  size_t merge_off = align_up(units_off + sizeof(PlanUnit) * units.size(), 32);
+  size_t total = align_up(merge_off + sizeof(PlanMerge) * merges.size(), 64);
+  if (total > (size_t)INT32_MAX) return set_error(MLA_ERR_INVALID_ARG, "plan too large");
+  if (plan_bytes_out) *plan_bytes_out = total;
+  if (workspace_bytes_out) *workspace_bytes_out = workspace_bytes_for(part_rows);
+  if (!plan_buf || plan_buf_bytes < total)
+    return set_error(MLA_ERR_BUFFER, "plan buffer needs %zu bytes (got %zu)", total, plan_buf ? plan_buf_bytes : (size_t)0);
+
+  uint8_t* base = (uint8_t*)plan_buf;
+  memset(base, 0, total);
+  PlanHeader h{};
+  h.magic = kPlanMagic; h.version = kPlanVersion;
+  h.batch = batch; h.num_heads = num_heads; h.kv_dtype = kv_dtype; h.total_q = (int32_t)total_q;
+  h.n_units = (int32_t)units.size(); h.n_merge = (int32_t)merges.size();
+  int used_cap = 0;
+  for (auto& u : units) used_cap = std::max(used_cap, u.nrows);
+  h.rows_cap = used_cap; h.n_part_rows = part_rows; h.max_pages = max_pages;
+  h.req_off = (int32_t)req_off; h.units_off = (int32_t)units_off; h.merge_off = (int32_t)merge_off;
+  h.total_bytes = (int32_t)total;
+  memcpy(base, &h, sizeof h);
+  memcpy(base + req_off, reqs.data(), sizeof(PlanRequest) * batch);
+  if (!units.empty()) memcpy(base + units_off, units.data(), sizeof(PlanUnit) * units.size());
+  if (!merges.empty()) memcpy(base + merge_off, merges.data(), sizeof(PlanMerge) * merges.size());
+  return MLA_OK;
+}
+
+extern "C" int mla_decode_plan(const int32_t* seq_lens_h, const int32_t* q_lens_h, int batch, int num_heads,
+                               int page_size, int kv_dtype, int num_sms, void* plan_buf, size_t plan_buf_bytes,
+                               size_t* plan_bytes_out, size_t* workspace_bytes_out) {
+  return mla_decode_plan_ex(seq_lens_h, q_lens_h, batch, num_heads, page_size, kv_dtype, num_sms, nullptr, plan_buf,
+                            plan_buf_bytes, plan_bytes_out, workspace_bytes_out);
+}
+
+namespace mla {
+
+int check_plan(const void* plan_host, size_t plan_bytes, const PlanHeader** out) {
+  if (!plan_host) return set_error(MLA_ERR_INVALID_ARG, "plan_host must not be NULL");
+  if (plan_bytes < sizeof(PlanHeader)) return set_error(MLA_ERR_PLAN, "plan is %zu bytes, smaller than its header", plan_bytes);
+  const PlanHeader* h = (const PlanHeader*)plan_host;
+  if (h->magic != kPlanMagic || h->version != kPlanVersion)
+    return set_error(MLA_ERR_PLAN, "plan bytes were not written by this library version");
+  if ((size_t)h->total_bytes != plan_bytes)
+    return set_error(MLA_ERR_PLAN, "plan_bytes %zu differs from the plan's size %d", plan_bytes, h->total_bytes);
+  *out = h;
+  return MLA_OK;
+}
+
+}  // namespace mla
+
+extern "C" int mla_decode_plan_info(const void* plan_host, size_t plan_bytes, int* n_units, int* n_merge,
+                                    int* total_q, int* num_heads, int* kv_dtype) {
+  clear_error();
+  const PlanHeader* h = nullptr;
+  int rc = check_plan(plan_host, plan_bytes, &h);
+  if (rc != MLA_OK) return rc;
+  if (n_units) *n_units = h->n_units;
+  if (n_merge) *n_merge = h->n_merge;
+  if (total_q) *total_q = h->total_q;
+  if (num_heads) *num_heads = h->num_heads;
+  if (kv_dtype) *kv_dtype = h->kv_dtype;
+  return MLA_OK;
+}

@@ -1,0 +1,159 @@
+"""GPU parity: the sm_103a path (through the C entry points) against the float64 oracle
+on the same seeded inputs, element by element, at sizes that span several pages,
+several splits and a ragged tail, plus the full-size workloads on sampled tokens."""
+import numpy as np
+import pytest
+import torch
+
+from mla_speculative_verify_gb300 import inputs
+from mla_speculative_verify_gb300.binding import PlanOptions
+from tests.gpu_util import assert_close, oracle_rows, run_gpu, run_oracle, to_device
+
+pytestmark = pytest.mark.gpu
+
+BF16, FP8 = inputs.KV_BF16, inputs.KV_FP8
+
+
+def _check(prob, options=None):
+    out, lse, _ = run_gpu(prob, options)
+    o_ref, l_ref = run_oracle(prob)
+    return assert_close(out, lse, o_ref, l_ref)
+
+
+def test_contiguous_h12_q2_ctx4096():
+    """The small contiguous workload at full size."""
+    _check(inputs.workload_contiguous_small())
+
+
+@pytest.mark.parametrize("q", [1, 2, 4, 8])
+@pytest.mark.parametrize("kv", [BF16, FP8])
+def test_h12_sweep_reduced_ctx(q, kv):
+    prob = inputs.make_problem(12, [9000 + 37], [q], kv, seed=2000 + q, poison_tail=True)
+    _check(prob)
+
+
+@pytest.mark.parametrize("q", [1, 8])
+@pytest.mark.parametrize("kv", [BF16, FP8])
+def test_h96_reduced_ctx(q, kv):
+    prob = inputs.make_problem(96, [3000 + 5], [q], kv, seed=2100 + q, poison_tail=True)
+    _check(prob)
+
+
+@pytest.mark.parametrize("H", [48, 128])
+@pytest.mark.parametrize("pattern", ["ragged", "uniform"])
+def test_ragged_batch_fp8_reduced(H, pattern):
+    prob = inputs.workload_ragged(H, pattern, B=32, ctx_lo=300, ctx_hi=900, seed=2200)
+    _check(prob)
+
+
+@pytest.mark.parametrize("seq,q,H", [([1], [1], 12), ([8], [8], 12), ([64], [3], 12), ([65], [2], 20),
+                                     ([130], [6], 7), ([200], [5], 128)])
+def test_edge_shapes(seq, q, H):
+    """ctx == q (only verify keys), one key, exactly one page, one key past a page,
+    odd head counts, H = 128."""
+    for kv in (BF16, FP8):
+        _check(inputs.make_problem(H, seq, q, kv, seed=2300 + seq[0], poison_tail=True))
+
+
+def test_many_splits_with_empty_causal_partials():
+    """One page per split: the last split holds keys that early verify rows may not see."""
+    prob = inputs.make_problem(12, [64 * 6 + 3], [8], BF16, seed=2400, poison_tail=True)
+    _check(prob, PlanOptions(force_splits=7))
+
+
+@pytest.mark.parametrize("kv", [BF16, FP8])
+def test_fold_less_mode_matches_fold(kv):
+    """F = 1 (one token per CTA tile) against the folded plan: same numbers within rounding."""
+    prob = inputs.make_problem(12, [5000], [4], kv, seed=2500)
+    o1, l1, _ = run_gpu(prob)
+    o2, l2, _ = run_gpu(prob, PlanOptions(force_fold=1))
+    o_ref, l_ref = run_oracle(prob)
+    assert_close(o1, l1, o_ref, l_ref)
+    assert_close(o2, l2, o_ref, l_ref)
+
+
+def test_unsplit_rows_are_bitwise_reproducible():
+    prob = inputs.make_problem(12, [3000], [4], BF16, seed=2600)
+    opts = PlanOptions(force_splits=1)
+    a = run_gpu(prob, opts)
+    b = run_gpu(prob, opts)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_split_replay_spread_is_small():
+    prob = inputs.make_problem(12, [20000], [8], BF16, seed=2700)
+    a = run_gpu(prob)
+    b = run_gpu(prob)
+    assert np.abs(a[0] - b[0]).max() <= 1e-3 and np.abs(a[1] - b[1]).max() <= 1e-5
+
+
+def test_graph_replay_with_changed_page_table():
+    """Capture one call in a CUDA graph, then permute the pages (cache and table
+    together) and replay: same result, no re-plan."""
+    from mla_speculative_verify_gb300.decoder import VerifyDecoder
+
+    prob = inputs.make_problem(12, [4000], [4], BF16, seed=2800, extra_pages=8)
+    dec = VerifyDecoder(prob.seq_lens, prob.q_lens, prob.H, prob.kv_dtype)
+    q, kv, pt = to_device(prob)
+    out = torch.zeros((prob.total_q, prob.H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((prob.total_q, prob.H), dtype=torch.float32, device="cuda")
+    dec.run(q, kv, pt, out, lse, prob.sm_scale)  # warm-up (sets kernel attributes)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            dec.run(q, kv, pt, out, lse, prob.sm_scale)
+    g.replay()
+    torch.cuda.synchronize()
+    o_ref, l_ref = run_oracle(prob)
+    assert_close(out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref)
+    # move every page to a new physical slot
+    n = prob.num_pages
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(5))
+    new_kv = torch.empty_like(kv)
+    new_kv.view(n, 64, 576)[perm.to("cuda")] = kv.view(n, 64, 576)
+    kv.copy_(new_kv)
+    pt.copy_(perm.to("cuda")[pt.long()].to(torch.int32))
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref)
+
+
+def test_plan_mismatch_is_reported_not_faulted():
+    from mla_speculative_verify_gb300.binding import MLA_DEVICE_PLAN_MISMATCH
+
+    prob = inputs.make_problem(12, [1000], [2], BF16, seed=2900)
+    from mla_speculative_verify_gb300.decoder import VerifyDecoder
+
+    dec = VerifyDecoder(prob.seq_lens, prob.q_lens, prob.H, prob.kv_dtype)
+    q, kv, pt = to_device(prob)
+    out = torch.zeros((prob.total_q, prob.H, 512), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wrong = torch.tensor([999], dtype=torch.int32, device="cuda")
+    dec.run(q, kv, pt, out, None, prob.sm_scale, 1.0, status, seq_lens_dev=wrong)
+    torch.cuda.synchronize()
+    assert int(status.item()) & MLA_DEVICE_PLAN_MISMATCH
+    # the context stays usable
+    out2, lse2, st = run_gpu(prob)
+    assert st == 0
+
+
+# ---------------------------------------------------------------- full sizes, sampled tokens
+@pytest.mark.parametrize("q", [1, 8])
+def test_full_size_h12_131k_sampled(q):
+    prob = inputs.workload_sweep_131k(q)
+    out, lse, _ = run_gpu(prob)
+    toks = sorted({0, q - 1})
+    o_ref, l_ref = oracle_rows(prob, toks)
+    assert_close(out[toks], lse[toks], o_ref, l_ref)
+
+
+@pytest.mark.parametrize("kv", [BF16, FP8])
+def test_full_size_h12_1m_sampled(kv):
+    prob = inputs.workload_long(kv)
+    out, lse, _ = run_gpu(prob)
+    toks = [0, 7]
+    o_ref, l_ref = oracle_rows(prob, toks)
+    assert_close(out[toks], lse[toks], o_ref, l_ref)

@@ -1,0 +1,165 @@
+"""Host-side tests of the C-ABI library: exports, planner invariants, argument checks.
+No GPU needed: the planner is host-only and mla_decode_run validates every argument
+before it touches the CUDA runtime."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from mla_speculative_verify_gb300 import binding
+from tests.plan_reader import read_plan
+
+KV = binding.MLA_KV_BF16
+
+
+def test_library_exports_every_declared_symbol():
+    lib = binding.load()
+    names = binding.declared_functions()
+    assert set(names) >= {"mla_decode_plan", "mla_decode_plan_ex", "mla_decode_plan_info", "mla_decode_run",
+                          "mla_last_error", "mla_version"}
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(binding.SIGNATURES) == set(names)
+    assert lib.mla_version() >= 100
+
+
+def _fold(q, H):
+    return max(f for f in range(1, q + 1) if q % f == 0 and H * f <= 128)
+
+
+CASES = [
+    ([4096], [2], 12), ([131072], [1], 12), ([131072], [8], 12), ([1 << 20], [8], 12), ([32768], [8], 96),
+    ([131072], [1], 96), ([20000, 17000, 30000, 16384], [1, 2, 3, 4], 48), ([25000] * 5, [4] * 5, 128),
+    ([1], [1], 1), ([8], [8], 12), ([65], [3], 7), ([64 * 5 + 1], [6], 20),
+]
+
+
+@pytest.mark.parametrize("seq_lens,q_lens,H", CASES)
+@pytest.mark.parametrize("num_sms", [152, 7])
+def test_plan_invariants(seq_lens, q_lens, H, num_sms):
+    buf, ws = binding.plan(seq_lens, q_lens, H, KV, num_sms)
+    p = read_plan(buf)
+    hd = p["header"]
+    assert hd["batch"] == len(seq_lens) and hd["num_heads"] == H and hd["total_q"] == sum(q_lens)
+    cu = np.concatenate([[0], np.cumsum(q_lens)])
+    # every (global row, key) pair is covered exactly once by the units
+    cover = {}
+    for u in p["units"]:
+        b = u["b"]
+        ctx = seq_lens[b]
+        assert 0 <= u["kv_begin"] < u["kv_end"] <= ctx
+        assert u["kv_begin"] % 64 == 0
+        assert u["kv_end"] % 64 == 0 or u["kv_end"] == ctx
+        assert 1 <= u["nrows"] <= 48
+        r0, r1 = u["qrow0"], u["qrow0"] + u["nrows"]
+        assert cu[b] * H <= r0 and r1 <= cu[b + 1] * H, "a unit's rows stay inside its request"
+        for r in range(r0, r1, max(1, (r1 - r0) // 3)):
+            cover.setdefault(r, []).append((u["kv_begin"], u["kv_end"]))
+    for r, spans in cover.items():
+        spans.sort()
+        b = int(np.searchsorted(cu, r // H, side="right") - 1)
+        assert spans[0][0] == 0 and spans[-1][1] == seq_lens[b]
+        for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+            assert a1 == b0
+    # fold groups: a unit's rows never straddle two fold groups
+    for u in p["units"]:
+        b = u["b"]
+        F = _fold(q_lens[b], H)
+        g0 = (u["qrow0"] // H - cu[b]) // F
+        g1 = ((u["qrow0"] + u["nrows"] - 1) // H - cu[b]) // F
+        assert g0 == g1
+        assert p["requests"][b]["fold"] == F
+    # merge items point at exactly the split units' partial rows
+    parts = sorted((u["part_row0"], u["nrows"]) for u in p["units"] if u["part_row0"] >= 0)
+    covered = sum(n for _, n in parts)
+    assert covered == hd["n_part_rows"]
+    for m in p["merges"]:
+        assert m["n_splits"] >= 2
+    assert ws == (0 if hd["n_part_rows"] == 0 else
+                  ((hd["n_part_rows"] * 512 * 4 + 255) // 256 * 256 + (hd["n_part_rows"] * 4 + 255) // 256 * 256))
+    # the units fill the SMs without leaving most of them idle
+    total_pages = sum(-(-s // 64) for s in seq_lens)
+    if total_pages >= 4 * num_sms:
+        assert len(p["units"]) >= num_sms // 2
+
+
+def test_plan_forced_splits_and_fold():
+    opts = binding.PlanOptions(force_splits=5, max_rows_per_cta=16, min_pages_per_split=0, force_fold=1)
+    buf, _ = binding.plan([1000], [4], 12, KV, 152, opts)
+    p = read_plan(buf)
+    assert all(u["nrows"] <= 16 for u in p["units"])
+    assert all(u["n_splits"] == 5 for u in p["units"])
+    assert p["requests"][0]["fold"] == 1
+    assert len(p["units"]) == 5 * 4  # 4 tokens x 12 heads = 4 tiles of 12 rows, 5 splits each
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(seq_lens=[10], q_lens=[11], H=12), binding.MLA_ERR_INVALID_ARG),
+    (dict(seq_lens=[10], q_lens=[0], H=12), binding.MLA_ERR_INVALID_ARG),
+    (dict(seq_lens=[10], q_lens=[1], H=0), binding.MLA_ERR_UNSUPPORTED),
+    (dict(seq_lens=[10], q_lens=[1], H=129), binding.MLA_ERR_UNSUPPORTED),
+    (dict(seq_lens=[10], q_lens=[1], H=12, page_size=32), binding.MLA_ERR_UNSUPPORTED),
+    (dict(seq_lens=[10], q_lens=[1], H=12, kv_dtype=7), binding.MLA_ERR_INVALID_ARG),
+    (dict(seq_lens=[10], q_lens=[1], H=12, num_sms=0), binding.MLA_ERR_INVALID_ARG),
+])
+def test_plan_rejects(args, code):
+    with pytest.raises(binding.MlaError) as e:
+        binding.plan(args["seq_lens"], args["q_lens"], args["H"], args.get("kv_dtype", KV), args.get("num_sms", 152),
+                     page_size=args.get("page_size", 64))
+    assert e.value.code == code
+    assert binding.last_error()
+
+
+def test_plan_buffer_too_small():
+    lib = binding.load()
+    s = np.array([100], np.int32)
+    q = np.array([2], np.int32)
+    nb, ws = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    small = np.zeros(16, np.uint8)
+    rc = lib.mla_decode_plan(s.ctypes.data_as(binding._I32P), q.ctypes.data_as(binding._I32P), 1, 12, 64, KV, 152,
+                             small.ctypes.data_as(ctypes.c_void_p), 16, ctypes.byref(nb), ctypes.byref(ws))
+    assert rc == binding.MLA_ERR_BUFFER and nb.value > 16
+
+
+def _run_args(plan, **over):
+    a = dict(plan_dev=0x10000, plan_host=plan, q=0x20000, kv=0x30000, pt=0x40000, stride=4, num_pages=8,
+             seq=0x50000, ql=0x60000, sm=0.07, kvs=1.0, out=0x70000, lse=0x80000, ws=None, ws_bytes=0, status=None)
+    a.update(over)
+    return a
+
+
+def _call_run(a):
+    lib = binding.load()
+    P = ctypes.c_void_p
+    ph = a["plan_host"]
+    return lib.mla_decode_run(P(a["plan_dev"]) if a["plan_dev"] else None, ph.ctypes.data_as(P), ph.nbytes,
+                              P(a["q"]) if a["q"] else None, P(a["kv"]), P(a["pt"]), a["stride"], a["num_pages"],
+                              P(a["seq"]), P(a["ql"]), a["sm"], a["kvs"], P(a["out"]),
+                              P(a["lse"]) if a["lse"] else None, P(a["ws"]) if a["ws"] else None, a["ws_bytes"],
+                              P(a["status"]) if a["status"] else None, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(plan_dev=0), binding.MLA_ERR_INVALID_ARG),
+    (dict(q=0), binding.MLA_ERR_INVALID_ARG),
+    (dict(q=0x20008), binding.MLA_ERR_INVALID_ARG),          # misaligned for TMA
+    (dict(lse=0x80002), binding.MLA_ERR_INVALID_ARG),
+    (dict(stride=1), binding.MLA_ERR_INVALID_ARG),            # shorter than the longest request
+    (dict(num_pages=0), binding.MLA_ERR_INVALID_ARG),
+    (dict(sm=0.0), binding.MLA_ERR_INVALID_ARG),
+    (dict(kvs=float("nan")), binding.MLA_ERR_INVALID_ARG),
+])
+def test_run_rejects_bad_arguments_before_any_launch(over, code):
+    plan, ws = binding.plan([200], [2], 12, KV, 152, binding.PlanOptions(force_splits=1))
+    assert ws == 0
+    assert _call_run(_run_args(plan, **over)) == code
+
+
+def test_run_rejects_small_workspace_and_foreign_plan():
+    plan, ws = binding.plan([20000], [2], 12, KV, 152)
+    assert ws > 0
+    assert _call_run(_run_args(plan, stride=400, ws=None, ws_bytes=0)) == binding.MLA_ERR_BUFFER
+    assert _call_run(_run_args(plan, stride=400, ws=0x100000, ws_bytes=ws - 1)) == binding.MLA_ERR_BUFFER
+    bad = plan.copy()
+    bad[:4] = 0
+    assert _call_run(_run_args(bad, stride=400)) == binding.MLA_ERR_PLAN
