@@ -4,27 +4,33 @@
 // (row = token * H + head; the q verify tokens of a fold group are folded into the
 // rows, sglang PR #33650 "Why" paragraph) against one page-aligned key range of
 // one request. The cache streams through shared memory once per unit, one 64-key
-// page per pipeline stage, and both products run on the tcgen05 tensor cores with
-// the accumulators in tensor memory, in the transposed orientation:
+// page per pipeline stage (one 3-D TMA box per page), and both products run on the
+// tcgen05 tensor cores with the accumulators in tensor memory, in the transposed
+// orientation:
 //
 //   S^T[key, row]  = K[key, 0:576] . Q[row, 0:576]^T    (M = 64 keys, N = rows, K = 576)
 //   O^T[dv, row]  += V^T[dv, key] . P^T[key, row]        (M = 128 dv x 4 blocks, N = rows, K = 64 keys)
 //
-// so the MMA N dimension is exactly the packed-row count (rounded up to 16) and no
-// MMA work is spent on padding rows up to 64 or 128. V^T is the same shared-memory
-// page as K, read MN-major (the latent cache rows hold V in columns 0..511; flashinfer
-// PR #5602 "What r52 changes": the latent K stages are held until PV).
+// so the MMA N dimension is the packed-row count rounded up to 16 and no MMA work is
+// spent on padding rows to 64 or 128. V^T is the same shared-memory page as K, read
+// MN-major (the latent cache rows hold V in columns 0..511; flashinfer PR #5602 "What
+// r52 changes": the latent K stages are held until PV).
 //
-// Warp roles (one CTA per SM, 1 KV page in flight while the other is consumed):
-//   warp 0     TMA producer: Q tile once, then one page per stage (9 boxes of 64x64)
-//   warp 1     TMEM owner and MMA issuer (one elected thread)
-//   warps 2-5  softmax: each thread owns one key of the S^T tile (a TMEM lane); online
-//              softmax with a lazy per-row reference: the reference moves (and O is
-//              rescaled in TMEM) only when a score exceeds it by kRefSlack octaves
-//              (the conditional-rescale idea of flashinfer PR #5602, deferred O rescale);
-//              then the epilogue: O / l to bf16 out and LSE, or fp32 partials
-//   warps 6-9  (fp8 cache only) convert the e4m3 page to bf16 in place (exact), the
-//              per-tensor scale folded into the score scale and the output scale
+// One thread issues a tcgen05.mma only every ~60 cycles, while an N = 16..48 MMA
+// needs 20..45 cycles of tensor time, so four warps issue in parallel: warp 1+p owns
+// K-chunks of the S^T product (into its own partial accumulator S_p, summed by the
+// softmax) and dv block p of the O^T product.
+//
+// Warp roles (one CTA per SM, one page in flight while the other is consumed):
+//   warp 0     TMA producer: the Q tile once, then one page per stage
+//   warps 1-4  MMA issue (one elected lane each); for an fp8 cache they first expand
+//              their own chunks of the e4m3 page to bf16 in place (exact; kv_scale is
+//              folded into the score and output scales)
+//   warps 5-8  softmax: each thread owns one key of the S^T tile (a TMEM lane); online
+//              softmax with a lazy per-row reference: the reference moves, and O^T is
+//              rescaled in TMEM, only when a score exceeds it by kRefSlack octaves (the
+//              conditional rescale of flashinfer PR #5602); then the epilogue: O / l to
+//              bf16 out and LSE, or fp32 partials for the merge kernel
 //
 // Every mbarrier wait is bounded; on expiry the kernel ORs MLA_DEVICE_WAIT_TIMEOUT into
 // the status word, stops the unit, drains its in-flight copies and frees its TMEM.
@@ -52,7 +58,7 @@ constexpr int kQChunkBytes = kRowsCap * 128;       // 6144
 constexpr int kQBytes = kChunks * kQChunkBytes;    // 55296
 constexpr int kKvChunkBytes = kTileKeys * 128;     // 8192
 constexpr int kSlotBytes = kChunks * kKvChunkBytes;  // 73728 (bf16 page)
-constexpr int kFp8StageOff = kSlotBytes / 2;       // e4m3 page lands in the upper half of its slot
+constexpr int kFp8StageOff = kSlotBytes / 2;       // an e4m3 page lands in the upper half of its slot
 constexpr int kFp8ChunkBytes = kTileKeys * 64;     // 4096
 constexpr int kPtBytes = kTileKeys * 128;          // P^T tile: 64 keys x (<= 64 rows) bf16
 constexpr int kOffQ = 0;
@@ -64,13 +70,19 @@ constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory");
 static_assert(kOffKv % 1024 == 0 && kOffPt % 1024 == 0 && kOffMisc % 1024 == 0, "1024-byte swizzle atoms");
 
+constexpr int kMmaWarps = 4;
+constexpr int kThreads = 32 * (1 + kMmaWarps + 4);  // producer, MMA warps, softmax warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;       // O^T block b at columns 64 b (N <= 64)
-constexpr uint32_t kTmemS = 256;     // S^T buffer i at columns 256 + 64 i
+constexpr uint32_t kTmemS = 256;     // partial S^T p at columns 256 + 64 p
 constexpr float kRefSlack = 8.0f;    // octaves a score may exceed the row reference before it moves
 constexpr long long kWaitBudget = 2000000000LL;  // cycles (~1 s) before a wait gives up
 
-// Rows of an M = 64 accumulator occupy TMEM lanes 16 per 32-lane quadrant:
+// K-chunks of the S^T product owned by MMA warp p: [chunk_lo(p), chunk_lo(p + 1)),
+// i.e. 3, 2, 2, 2 of the 9 chunks.
+__host__ __device__ __forceinline__ int chunk_lo(int p) { return p == 0 ? 0 : 1 + 2 * p; }
+
+// Rows of an M = 64 accumulator occupy 16 TMEM lanes per 32-lane quadrant:
 // row r -> lane 32 * (r / 16) + r % 16.
 __device__ __forceinline__ int m64_row_of_lane(int quadrant, int lane) { return lane < 16 ? quadrant * 16 + lane : -1; }
 
@@ -91,10 +103,11 @@ struct Params {
 
 struct Misc {
   uint64_t bar_q;
-  uint64_t kv_full[2], kv_ready[2], kv_empty[2];
-  uint64_t s_full[2], s_empty[2], p_full[2], pt_empty[2];
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t s_full, s_empty;
+  uint64_t p_full[2], pt_empty[2];
   uint64_t mma_done;
-  uint64_t grp_softmax, grp_dequant;  // bounded barriers among the 4 warps of a group
+  uint64_t grp_softmax, grp_mma;  // bounded barriers among the 4 warps of a group
   uint32_t tmem_base;
   int abort;
   int unit[8];
@@ -171,7 +184,7 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint3
 }
 
 template <bool kFp8>
-__global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     fold_decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv, Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -194,16 +207,15 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
     ptx::mbar_init(&ms->bar_q, 1);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&ms->kv_full[i], 1);
-      ptx::mbar_init(&ms->kv_ready[i], 4);
-      ptx::mbar_init(&ms->kv_empty[i], 1);
-      ptx::mbar_init(&ms->s_full[i], 1);
-      ptx::mbar_init(&ms->s_empty[i], 4);
+      ptx::mbar_init(&ms->kv_empty[i], kMmaWarps);
       ptx::mbar_init(&ms->p_full[i], 4);
-      ptx::mbar_init(&ms->pt_empty[i], 1);
+      ptx::mbar_init(&ms->pt_empty[i], kMmaWarps);
     }
-    ptx::mbar_init(&ms->mma_done, 1);
+    ptx::mbar_init(&ms->s_full, kMmaWarps);
+    ptx::mbar_init(&ms->s_empty, 4);
+    ptx::mbar_init(&ms->mma_done, kMmaWarps);
     ptx::mbar_init(&ms->grp_softmax, 4);
-    ptx::mbar_init(&ms->grp_dequant, 4);
+    ptx::mbar_init(&ms->grp_mma, kMmaWarps);
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -234,11 +246,8 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
       if (lane == 0) {
         ptx::prefetch_tmap(&tmap_q);
         ptx::prefetch_tmap(&tmap_kv);
-        const int nbox = nmma / 16;
-        ptx::mbar_arrive_expect_tx(&ms->bar_q, kChunks * nbox * 16 * 128);
-        for (int c = 0; c < kChunks; ++c)
-          for (int r = 0; r < nbox; ++r)
-            ptx::tma_load_2d(sQ + c * kQChunkBytes + r * 2048, &tmap_q, &ms->bar_q, 64 * c, qrow0 + 16 * r);
+        ptx::mbar_arrive_expect_tx(&ms->bar_q, kQBytes);
+        ptx::tma_load_3d(sQ, &tmap_q, &ms->bar_q, 0, qrow0, 0);
       }
       const int32_t* pt_row = p.page_table + (size_t)b * p.pt_stride + kv_begin / kPage;
       for (int t0 = 0; t0 < ntiles && !*abort; t0 += 32) {
@@ -261,13 +270,10 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
               uint8_t* dst = sKv + slot * kSlotBytes;
               if (kFp8) {
                 ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], kChunks * kFp8ChunkBytes);
-                for (int c = 0; c < kChunks; ++c)
-                  ptx::tma_load_2d(dst + kFp8StageOff + c * kFp8ChunkBytes, &tmap_kv, &ms->kv_full[slot], 64 * c,
-                                   page * kPage);
+                ptx::tma_load_3d(dst + kFp8StageOff, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0);
               } else {
-                ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], kChunks * kKvChunkBytes);
-                for (int c = 0; c < kChunks; ++c)
-                  ptx::tma_load_2d(dst + c * kKvChunkBytes, &tmap_kv, &ms->kv_full[slot], 64 * c, page * kPage);
+                ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], kSlotBytes);
+                ptx::tma_load_3d(dst, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0);
               }
             }
           }
@@ -277,8 +283,8 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
         }
       }
     }
-    // Drain: every issued copy must have landed before the CTA may exit (at most the
-    // last two pages can still be in flight; earlier ones were consumed by the MMAs).
+    // Drain: every issued copy must land before the CTA may exit (at most the last two
+    // pages can still be in flight; earlier ones were consumed by the MMAs).
     if (lane == 0) {
       for (int t = max(0, issued - 2); t < issued; ++t) {
         long long t0c = clock64();
@@ -291,62 +297,114 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && !*abort) {
-      const uint32_t sq = ptx::smem_addr(sQ), skv = ptx::smem_addr(sKv), spt = ptx::smem_addr(sPt);
-      const uint32_t idesc_s = ptx::idesc_bf16(64, nmma, 0, 0);    // S^T: K-major K tile, K-major Q
-      const uint32_t idesc_o = ptx::idesc_bf16(128, nmma, 1, 1);   // O^T: MN-major V^T, MN-major P^T
-      bool ok = wait_bar(&ms->bar_q, 0, abort, p.status);
-      for (int t = 0; ok && t <= ntiles; ++t) {
-        if (t < ntiles) {
-          const int slot = t & 1;
-          ok = wait_bar(kFp8 ? &ms->kv_ready[slot] : &ms->kv_full[slot], (t >> 1) & 1, abort, p.status);
-          if (ok && t >= 2) ok = wait_bar(&ms->s_empty[slot], ((t - 2) >> 1) & 1, abort, p.status);
+  } else if (warp <= kMmaWarps) {
+    // ------------------------------------------------------------ MMA issue (+ fp8 expand)
+    const int pw = warp - 1;                   // 0..3
+    const int c_lo = chunk_lo(pw), c_hi = chunk_lo(pw + 1);
+    const uint32_t sq = ptx::smem_addr(sQ), skv = ptx::smem_addr(sKv), spt = ptx::smem_addr(sPt);
+    const uint32_t idesc_s = ptx::idesc_bf16(64, nmma, 0, 0);    // S^T: K-major K tile, K-major Q
+    const uint32_t idesc_o = ptx::idesc_bf16(128, nmma, 1, 1);   // O^T: MN-major V^T, MN-major P^T
+    const uint32_t d_s = tmem + kTmemS + 64 * pw, d_o = tmem + kTmemO + 64 * pw;
+    uint32_t gphase = 0;
+    bool ok = !*abort && warp_wait(&ms->bar_q, 0, abort, p.status);
+    bool issued_any = false;
+    for (int t = 0; ok && t <= ntiles; ++t) {
+      if (t < ntiles) {
+        const int slot = t & 1;
+        ok = warp_wait(&ms->kv_full[slot], (t >> 1) & 1, abort, p.status);
+        if (!ok) break;
+        if (kFp8) {
+          // this warp's chunks: read every e4m3 byte first (the bf16 rows overwrite the
+          // e4m3 staging area of other chunks), then write the bf16 rows
+          uint8_t* base = sKv + slot * kSlotBytes;
+          const int k = lane * 2;  // keys 2 lane, 2 lane + 1
+          uint4 raw[3][2][4];
+#pragma unroll
+          for (int ci = 0; ci < 3; ++ci)
+            if (c_lo + ci < c_hi)
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  raw[ci][kk][j] = *reinterpret_cast<const uint4*>(base + kFp8StageOff + (c_lo + ci) * kFp8ChunkBytes +
+                                                                   (k + kk) * 64 + 16 * j);
+          ok = group_sync(&ms->grp_mma, gphase, abort, p.status);
           if (!ok) break;
-          ptx::tc_fence_after();
+#pragma unroll
+          for (int ci = 0; ci < 3; ++ci)
+            if (c_lo + ci < c_hi)
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk) {
+                uint8_t* line = base + (c_lo + ci) * kKvChunkBytes + (k + kk) * 128;
+                const int sw = (k + kk) & 7;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  uint4 o0, o1;
+                  e4m3x4_to_bf16x4(raw[ci][kk][j].x, o0.x, o0.y);
+                  e4m3x4_to_bf16x4(raw[ci][kk][j].y, o0.z, o0.w);
+                  e4m3x4_to_bf16x4(raw[ci][kk][j].z, o1.x, o1.y);
+                  e4m3x4_to_bf16x4(raw[ci][kk][j].w, o1.z, o1.w);
+                  *reinterpret_cast<uint4*>(line + (((2 * j) ^ sw) << 4)) = o0;
+                  *reinterpret_cast<uint4*>(line + (((2 * j + 1) ^ sw) << 4)) = o1;
+                }
+              }
+          ptx::fence_async_smem();
+          __syncwarp();
+        }
+        if (t >= 1) {
+          ok = warp_wait(&ms->s_empty, (t - 1) & 1, abort, p.status);  // the softmax has read S(t-1)
+          if (!ok) break;
+        }
+        ptx::tc_fence_after();
+        if (lane == 0) {
           const uint32_t a0 = skv + slot * kSlotBytes;
-          const uint32_t d = tmem + kTmemS + 64 * slot;
-#pragma unroll 1
-          for (int c = 0; c < kChunks; ++c) {
+          for (int c = c_lo; c < c_hi; ++c) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               uint64_t ad = ptx::smem_desc(a0 + c * kKvChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
               uint64_t bd = ptx::smem_desc(sq + c * kQChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
-              ptx::mma_bf16_ss(d, ad, bd, idesc_s, (c | k) != 0);
+              ptx::mma_bf16_ss(d_s, ad, bd, idesc_s, (c != c_lo || k != 0) ? 1u : 0u);
             }
           }
-          ptx::mma_commit(&ms->s_full[slot]);
+          ptx::mma_commit(&ms->s_full);
         }
-        if (t >= 1) {
-          const int u = t - 1, ub = u & 1;
-          ok = wait_bar(&ms->p_full[ub], (u >> 1) & 1, abort, p.status);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          const uint32_t v0 = skv + ub * kSlotBytes, pt0 = spt + ub * kPtBytes;
-#pragma unroll 1
-          for (int blk = 0; blk < 4; ++blk) {
+        issued_any = true;
+        __syncwarp();
+      }
+      if (t >= 1) {
+        const int u = t - 1, ub = u & 1;
+        ok = warp_wait(&ms->p_full[ub], (u >> 1) & 1, abort, p.status);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t v0 = skv + ub * kSlotBytes + 2 * pw * kKvChunkBytes, pt0 = spt + ub * kPtBytes;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint64_t ad = ptx::smem_desc(v0 + 2 * blk * kKvChunkBytes + 2048 * k, kKvChunkBytes, 1024, ptx::kSwizzle128B);
-              uint64_t bd = ptx::smem_desc(pt0 + 2048 * k, 8192, 1024, ptx::kSwizzle128B);
-              ptx::mma_bf16_ss(tmem + kTmemO + 64 * blk, ad, bd, idesc_o, (u > 0 || k > 0) ? 1u : 0u);
-            }
+          for (int k = 0; k < 4; ++k) {
+            uint64_t ad = ptx::smem_desc(v0 + 2048 * k, kKvChunkBytes, 1024, ptx::kSwizzle128B);
+            uint64_t bd = ptx::smem_desc(pt0 + 2048 * k, 8192, 1024, ptx::kSwizzle128B);
+            ptx::mma_bf16_ss(d_o, ad, bd, idesc_o, (u > 0 || k > 0) ? 1u : 0u);
           }
           ptx::mma_commit(&ms->kv_empty[ub]);
           ptx::mma_commit(&ms->pt_empty[ub]);
         }
-      }
-      // all issued MMAs must retire before TMEM is released
-      ptx::mma_commit(&ms->mma_done);
-      long long t0c = clock64();
-      while (!ptx::mbar_try_wait(&ms->mma_done, 0) && clock64() - t0c < kWaitBudget) {
+        __syncwarp();
       }
     }
-  } else if (warp < 6) {
+    // every MMA this warp issued must retire before TMEM is released
+    if (issued_any) {
+      if (lane == 0) {
+        ptx::mma_commit(&ms->mma_done);
+        long long t0c = clock64();
+        while (!ptx::mbar_try_wait(&ms->mma_done, 0) && clock64() - t0c < kWaitBudget) {
+          if (*abort) break;  // the other MMA warps may not commit; the tensor core drains anyway
+        }
+      }
+      __syncwarp();
+    }
+  } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int qd = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int sidx = tid - 64;               // 0..127
+    const int sidx = tid - 32 * (kMmaWarps + 1);   // 0..127
     const int krow = m64_row_of_lane(qd, lane);
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     uint32_t gphase = 0;
@@ -365,17 +423,30 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
     for (int n = 0; n < kRowsCap; ++n) l_acc[n] = 0.f;
     for (int t = 0; ok && t < ntiles; ++t) {
       const int sb = t & 1;
-      ok = warp_wait(&ms->s_full[sb], (t >> 1) & 1, abort, p.status);
+      ok = warp_wait(&ms->s_full, t & 1, abort, p.status);
       if (!ok) break;
       ptx::tc_fence_after();
+      // S^T = sum of the four partial accumulators
       float x[kRowsCap];
 #pragma unroll
-      for (int c = 0; c < kRowsCap / 16; ++c)
-        if (c < nch) ptx::tmem_ld16(tmem + kTmemS + 64 * sb + lane_off + 16 * c, x + 16 * c);
-      ptx::tmem_ld_wait();
+      for (int c = 0; c < kRowsCap / 16; ++c) {
+        if (c < nch) {
+          float y[2][16];
+          ptx::tmem_ld16(tmem + kTmemS + lane_off + 16 * c, x + 16 * c);
+          ptx::tmem_ld16(tmem + kTmemS + 64 + lane_off + 16 * c, y[0]);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) x[16 * c + j] += y[0][j];
+          ptx::tmem_ld16(tmem + kTmemS + 128 + lane_off + 16 * c, y[0]);
+          ptx::tmem_ld16(tmem + kTmemS + 192 + lane_off + 16 * c, y[1]);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) x[16 * c + j] += y[0][j] + y[1][j];
+        }
+      }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&ms->s_empty[sb]);
+      if (lane == 0) ptx::mbar_arrive(&ms->s_empty);
       const int key = kv_begin + t * kTileKeys + krow;
       const bool valid = krow >= 0 && key < kv_end;
       bool need = false;
@@ -529,47 +600,6 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
         }
       }
     }
-  } else if (kFp8) {
-    // ------------------------------------------------------------ e4m3 -> bf16 (in place)
-    const int didx = tid - 192;        // 0..127
-    const int k = didx >> 1, half = didx & 1;
-    uint32_t gphase = 0;
-    bool ok = !*abort;
-    for (int t = 0; ok && t < ntiles; ++t) {
-      const int slot = t & 1;
-      ok = warp_wait(&ms->kv_full[slot], (t >> 1) & 1, abort, p.status);
-      if (!ok) break;
-      uint8_t* base = sKv + slot * kSlotBytes;
-      uint4 raw[kChunks][2];
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        const uint8_t* src = base + kFp8StageOff + c * kFp8ChunkBytes + k * 64 + half * 32;
-        raw[c][0] = *reinterpret_cast<const uint4*>(src);
-        raw[c][1] = *reinterpret_cast<const uint4*>(src + 16);
-      }
-      // every e4m3 byte of the page is read before any bf16 byte is written over it
-      ok = group_sync(&ms->grp_dequant, gphase, abort, p.status);
-      if (!ok) break;
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        uint8_t* line = base + c * kKvChunkBytes + k * 128;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint4 w = raw[c][h];
-          uint4 o0, o1;
-          e4m3x4_to_bf16x4(w.x, o0.x, o0.y);
-          e4m3x4_to_bf16x4(w.y, o0.z, o0.w);
-          e4m3x4_to_bf16x4(w.z, o1.x, o1.y);
-          e4m3x4_to_bf16x4(w.w, o1.z, o1.w);
-          const int j0 = half * 4 + h * 2;  // 16-byte chunk index within the 128-byte row
-          *reinterpret_cast<uint4*>(line + (((j0) ^ (k & 7)) << 4)) = o0;
-          *reinterpret_cast<uint4*>(line + (((j0 + 1) ^ (k & 7)) << 4)) = o1;
-        }
-      }
-      ptx::fence_async_smem();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&ms->kv_ready[slot]);
-    }
   }
 
   ptx::tc_fence_before();
@@ -581,57 +611,94 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
 }
 
 // ------------------------------------------------------------------ LSE merge
-// One warp per packed row: L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s
-// (a split a causal row cannot see has L_s = -inf and is skipped).
-__global__ void __launch_bounds__(128) lse_merge_kernel(const uint8_t* plan, const float* part_o, const float* part_lse,
-                                                       __nv_bfloat16* out, float* lse) {
+// One CTA per (packed row, quarter of the 512 value columns): 8 warps share the
+// splits of the row. L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s; a split that
+// a causal row cannot see has L_s = -inf and weight 0.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeMaxSplits = 2048;
+
+__global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const uint8_t* plan, const float* part_o,
+                                                                 const float* part_lse, __nv_bfloat16* out, float* lse) {
   ptx::pdl_wait_primary();
+  __shared__ float w_s[kMergeMaxSplits];
+  __shared__ float red[8][2];
+  __shared__ float4 acc_s[8][32];
   const PlanHeader* ph = (const PlanHeader*)plan;
   const PlanMerge m = ((const PlanMerge*)(plan + ph->merge_off))[blockIdx.y];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + warp;
+  const int row = blockIdx.x >> 2, quarter = blockIdx.x & 3;
   if (row >= m.nrows) return;
-  const int ns = m.n_splits;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ns = m.n_splits;  // the planner keeps this <= kMergeMaxSplits
+  // 1. L over the splits
   float mx = -INFINITY;
-  for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, part_lse[m.part_row0 + s * m.nrows + row]);
+  for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
+    const float v = part_lse[m.part_row0 + s * m.nrows + row];
+    w_s[s] = v;
+    mx = fmaxf(mx, v);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red[warp][0] = mx;
+  __syncthreads();
+  mx = red[0][0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i][0]);
   float sum = 0.f;
-  for (int s = lane; s < ns; s += 32) {
-    const float v = part_lse[m.part_row0 + s * m.nrows + row];
-    if (v != -INFINITY) sum += __expf(v - mx);
+  for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
+    const float v = w_s[s];
+    sum += v == -INFINITY ? 0.f : __expf(v - mx);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) red[warp][1] = sum;
+  __syncthreads();
+  sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sum += red[i][1];
   const float L = mx + __logf(sum);
-  float4 acc[4];
+  for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
+    const float v = w_s[s];
+    w_s[s] = v == -INFINITY ? 0.f : __expf(v - L);
+  }
+  __syncthreads();
+  // 2. weighted sum: warp w takes splits w, w+8, ...; each lane takes 4 consecutive columns
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int col = quarter * 128 + 4 * lane;
+  int s = warp;
+  for (; s + 8 < ns; s += 16) {
+    const float4 a = *reinterpret_cast<const float4*>(part_o + (size_t)(m.part_row0 + s * m.nrows + row) * kDv + col);
+    const float4 c = *reinterpret_cast<const float4*>(part_o + (size_t)(m.part_row0 + (s + 8) * m.nrows + row) * kDv + col);
+    const float wa = w_s[s], wc = w_s[s + 8];
+    acc.x += wa * a.x + wc * c.x; acc.y += wa * a.y + wc * c.y;
+    acc.z += wa * a.z + wc * c.z; acc.w += wa * a.w + wc * c.w;
+  }
+  for (; s < ns; s += 8) {
+    const float4 a = *reinterpret_cast<const float4*>(part_o + (size_t)(m.part_row0 + s * m.nrows + row) * kDv + col);
+    const float wa = w_s[s];
+    acc.x += wa * a.x; acc.y += wa * a.y; acc.z += wa * a.z; acc.w += wa * a.w;
+  }
+  acc_s[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    float4 r = acc_s[0][lane];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < ns; ++s) {
-    const int pr = m.part_row0 + s * m.nrows + row;
-    const float v = part_lse[pr];
-    if (v == -INFINITY) continue;
-    const float w = __expf(v - L);
-    const float4* src = reinterpret_cast<const float4*>(part_o + (size_t)pr * kDv);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float4 x = src[j * 32 + lane];
-      acc[j].x += w * x.x; acc[j].y += w * x.y; acc[j].z += w * x.z; acc[j].w += w * x.w;
+    for (int i = 1; i < 8; ++i) {
+      const float4 v = acc_s[i][lane];
+      r.x += v.x; r.y += v.y; r.z += v.z; r.w += v.w;
     }
+    const int qr = m.qrow0 + row;
+    uint2 pk = make_uint2(pack_bf16(r.x, r.y), pack_bf16(r.z, r.w));
+    *reinterpret_cast<uint2*>(out + (size_t)qr * kDv + col) = pk;
+    if (lse && quarter == 0 && lane == 0) lse[qr] = L;
   }
-  const int qr = m.qrow0 + row;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint2 pk = make_uint2(pack_bf16(acc[j].x, acc[j].y), pack_bf16(acc[j].z, acc[j].w));
-    *reinterpret_cast<uint2*>(out + (size_t)qr * kDv + 4 * (j * 32 + lane)) = pk;
-  }
-  if (lse && lane == 0) lse[qr] = L;
 }
 
 int rows_cap_for(int kv_dtype) {
   (void)kv_dtype;
   return kRowsCap;
 }
+
+int max_splits_for_merge() { return kMergeMaxSplits; }
 
 // ------------------------------------------------------------------ host side
 size_t workspace_bytes_for(int n_part_rows);
@@ -682,6 +749,21 @@ static int prepare_device(int dev) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Tensor map of a [rows, 576] matrix viewed as (64 columns, rows, 9 column chunks): one
+// box of (64, box_rows, 9) lands in shared memory as [chunk][row][64 columns].
+static CUresult encode_chunked(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const void* base, bool fp8,
+                               uint64_t rows, uint32_t box_rows) {
+  const uint64_t esz = fp8 ? 1 : 2;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)kChunks};
+  cuuint64_t strides[2] = {(cuuint64_t)(kDqk * esz), (cuuint64_t)(64 * esz)};
+  cuuint32_t box[3] = {64, box_rows, (cuuint32_t)kChunks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 }  // namespace mla
 
 using namespace mla;
@@ -722,29 +804,12 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encoder();
   if (!enc) return set_error(MLA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
 
-  alignas(64) CUtensorMap tq, tkv;
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)kDqk, (cuuint64_t)h->total_q * (cuuint64_t)h->num_heads};
-    cuuint64_t strides[1] = {(cuuint64_t)kDqk * 2};
-    cuuint32_t box[2] = {64, 16};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return set_error(MLA_ERR_CUDA, "tensor map for q failed (CUresult %d)", (int)r);
-  }
   const bool fp8 = h->kv_dtype == MLA_KV_FP8_E4M3;
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)kDqk, (cuuint64_t)num_pages * kPage};
-    cuuint64_t strides[1] = {(cuuint64_t)kDqk * (fp8 ? 1 : 2)};
-    cuuint32_t box[2] = {64, 64};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = enc(&tkv, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                     const_cast<void*>(kv_cache), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return set_error(MLA_ERR_CUDA, "tensor map for kv_cache failed (CUresult %d)", (int)r);
-  }
+  alignas(64) CUtensorMap tq, tkv;
+  CUresult r = encode_chunked(enc, &tq, q, false, (uint64_t)h->total_q * (uint64_t)h->num_heads, kRowsCap);
+  if (r != CUDA_SUCCESS) return set_error(MLA_ERR_CUDA, "tensor map for q failed (CUresult %d)", (int)r);
+  r = encode_chunked(enc, &tkv, kv_cache, fp8, (uint64_t)num_pages * kPage, kTileKeys);
+  if (r != CUDA_SUCCESS) return set_error(MLA_ERR_CUDA, "tensor map for kv_cache failed (CUresult %d)", (int)r);
 
   Params prm;
   prm.plan = (const uint8_t*)plan_dev;
@@ -765,15 +830,15 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
   prm.status = status_dev;
   cudaStream_t st = (cudaStream_t)stream;
   if (fp8)
-    fold_decode_kernel<true><<<h->n_units, 320, kSmemBytes, st>>>(tq, tkv, prm);
+    fold_decode_kernel<true><<<h->n_units, kThreads, kSmemBytes, st>>>(tq, tkv, prm);
   else
-    fold_decode_kernel<false><<<h->n_units, 192, kSmemBytes, st>>>(tq, tkv, prm);
+    fold_decode_kernel<false><<<h->n_units, kThreads, kSmemBytes, st>>>(tq, tkv, prm);
   ce = cudaGetLastError();
   if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "fold kernel launch: %s", cudaGetErrorString(ce));
   if (h->n_merge > 0) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((h->rows_cap + 3) / 4), (unsigned)h->n_merge, 1);
-    cfg.blockDim = dim3(128, 1, 1);
+    cfg.gridDim = dim3((unsigned)(h->rows_cap * 4), (unsigned)h->n_merge, 1);
+    cfg.blockDim = dim3(kMergeThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

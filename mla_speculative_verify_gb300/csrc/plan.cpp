@@ -26,6 +26,7 @@
 namespace mla {
 
 int rows_cap_for(int kv_dtype);  // defined next to the kernel
+int max_splits_for_merge();       // defined next to the merge kernel
 
 static int fold_factor(int q, int H) {
   int best = 1;
@@ -125,7 +126,7 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
     while (j < tiles.size() && tiles[j].b == b && grp_rows < R) { grp_rows += tiles[j].nrows; ++j; }
     int pages = tiles[i].pages;
     int n_split = o.force_splits > 0 ? o.force_splits : (int)((pages + per_unit - 1) / per_unit);
-    n_split = std::max(1, std::min(n_split, pages));
+    n_split = std::max(1, std::min(std::min(n_split, pages), max_splits_for_merge()));
     std::vector<int> part0(j - i, -1);
     if (n_split > 1) {
       for (size_t t = i; t < j; ++t) {

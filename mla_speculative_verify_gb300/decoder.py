@@ -27,6 +27,8 @@ class VerifyDecoder:
     def __init__(self, seq_lens, q_lens, num_heads: int, kv_dtype: str, device="cuda", num_sms: int | None = None,
                  options: binding.PlanOptions | None = None):
         self.device = torch.device(device)
+        if self.device.type == "cuda" and self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
         if kv_dtype not in KV_DTYPES:
             raise ValueError(f"kv_dtype must be one of {list(KV_DTYPES)}")
         self.kv_dtype = kv_dtype
