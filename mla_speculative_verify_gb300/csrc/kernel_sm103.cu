@@ -39,6 +39,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include <mutex>
@@ -78,8 +79,11 @@ constexpr uint32_t kTmemS = 256;     // partial S^T p at columns 256 + 64 p
 constexpr float kRefSlack = 8.0f;    // octaves a score may exceed the row reference before it moves
 constexpr long long kWaitBudget = 2000000000LL;  // cycles (~1 s) before a wait gives up
 
-// K-chunks of the S^T product owned by MMA warp p: [chunk_lo(p), chunk_lo(p + 1)),
-// i.e. 3, 2, 2, 2 of the 9 chunks.
+// K-steps (16 columns each) of the S^T product owned by MMA warp p: [9 p, 9 p + 9) of
+// the 36; the e4m3 expansion of a page is split by 64-column chunks instead
+// ([chunk_lo(p), chunk_lo(p + 1)) = 3, 2, 2, 2 of the 9 chunks).
+constexpr int kKSteps = kChunks * 4;
+constexpr int kKStepsPerWarp = kKSteps / 4;
 __host__ __device__ __forceinline__ int chunk_lo(int p) { return p == 0 ? 0 : 1 + 2 * p; }
 
 // Rows of an M = 64 accumulator occupy 16 TMEM lanes per 32-lane quadrant:
@@ -113,12 +117,13 @@ struct Misc {
   int unit[8];
   int req[4];
   int flags[2][4];
-  float ref[64];
-  float alpha[64];
-  int lim[64];
-  float colred[4][64];
-  float lsum[64];
+  alignas(16) float ref[64];  // read as float4
+  alignas(16) float alpha[64];
+  alignas(16) int lim[64];
+  alignas(16) float colred[4][64];
+  alignas(16) float lsum[64];
 };
+static_assert(offsetof(Misc, ref) % 16 == 0, "float4 reads of ref need 16-byte alignment");
 static_assert(sizeof(Misc) <= kMiscBytes, "misc block too small");
 
 __device__ __forceinline__ void report(int32_t* status, int bits) {
@@ -173,8 +178,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// e4m3 x4 (one 32-bit word) -> bf16 x4 (two 32-bit words), exact.
-__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+// e4m3 x4 (one 32-bit word) -> bf16 x4 (two 32-bit words), exact, through the
+// hardware conversions (used for words that hold a zero, subnormal or NaN code). Kept
+// out of line so that the common path below stays a branch, not a predicated copy.
+__device__ __noinline__ void e4m3x4_to_bf16x4_cvt(uint32_t w, uint32_t& lo, uint32_t& hi) {
   __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
   __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
   float2 f0 = __half22float2(*reinterpret_cast<__half2*>(&h0));
@@ -183,11 +190,260 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint3
   hi = pack_bf16(f1.x, f1.y);
 }
 
+// e4m3 x4 -> bf16 x4 with integer operations. A normal e4m3 code s.eeee.mmm equals
+// (-1)^s 2^(e-7) (1 + m/8); the bf16 with exponent field e + 120 and mantissa m << 4 holds
+// the same value, so each 16-bit half is ((c & 0x7F) << 4) + (120 << 7) with the sign
+// moved to bit 15. Codes with e = 0 (zero, subnormals) and the NaN codes S.1111.111
+// take the conversion path.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t ex = w & 0x78787878u;                  // zero byte <=> zero exponent
+  const uint32_t nn = (w & 0x7F7F7F7Fu) ^ 0x7F7F7F7Fu;  // zero byte <=> NaN code
+  if ((((ex - 0x01010101u) & ~ex) | ((nn - 0x01010101u) & ~nn)) & 0x80808080u) {
+    e4m3x4_to_bf16x4_cvt(w, lo, hi);
+    return;
+  }
+  const uint32_t a = __byte_perm(w, 0u, 0x4140);  // codes 0, 1 in the low bytes of the halves
+  const uint32_t b = __byte_perm(w, 0u, 0x4342);  // codes 2, 3
+  lo = (((a & 0x007F007Fu) << 4) + 0x3C003C00u) | ((a & 0x00800080u) << 8);
+  hi = (((b & 0x007F007Fu) << 4) + 0x3C003C00u) | ((b & 0x00800080u) << 8);
+}
+
+
+struct SoftmaxArgs {
+  Misc* ms;
+  uint8_t* sKv;
+  uint8_t* sPt;
+  uint32_t tmem;
+  int qd, lane, sidx, nrows, qrow0, kv_begin, kv_end, ntiles, part_row0, ctx, qlen, tok0;
+  volatile int* abort;
+};
+
+// Softmax warps for a tile of 16 NCH packed rows. Lanes 0..15 of a warp read their key's
+// S^T row from TMEM (the M = 64 accumulator uses 16 lanes per quadrant) and hand the
+// upper 8 of every 16 columns to lanes 16..31, so each thread works on 8 NCH columns of
+// one key: columns 16 c + 8 half + j, c < NCH, j < 8.
+template <int NCH>
+__device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params& p) {
+  constexpr int NC = 8 * NCH;
+  Misc* ms = a.ms;
+  const int lane = a.lane, qd = a.qd, sidx = a.sidx;
+  const int half = lane >> 4;
+  const int krow = qd * 16 + (lane & 15);  // key row of this thread in the 64-key tile
+  const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+  volatile int* abort = a.abort;
+  uint32_t gphase = 0;
+  if (sidx < 64) {
+    int lim = 0;
+    if (sidx < a.nrows) {
+      const int i = (a.qrow0 + sidx) / p.H - a.tok0;  // verify token of this packed row
+      lim = a.ctx - a.qlen + i + 1;
+    }
+    ms->lim[sidx] = lim;
+    ms->ref[sidx] = -INFINITY;
+  }
+  bool ok = group_sync(&ms->grp_softmax, gphase, abort, p.status) && !*abort;
+  int lim_min = a.kv_end;
+  for (int n = 0; n < a.nrows; ++n) lim_min = min(lim_min, ms->lim[n]);
+  float l_acc[NC];
+#pragma unroll
+  for (int i = 0; i < NC; ++i) l_acc[i] = 0.f;
+  const float scale = p.score_scale_log2;
+  for (int t = 0; ok && t < a.ntiles; ++t) {
+    const int sb = t & 1;
+    ok = warp_wait(&ms->s_full, t & 1, abort, p.status);
+    if (!ok) break;
+    ptx::tc_fence_after();
+    // S^T = sum of the four partial accumulators, then split the columns over the halves
+    float x[NC];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      float s0[16], s1[16], s2[16];
+      ptx::tmem_ld16(a.tmem + kTmemS + lane_off + 16 * c, s0);
+      ptx::tmem_ld16(a.tmem + kTmemS + 64 + lane_off + 16 * c, s1);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) s0[j] += s1[j];
+      ptx::tmem_ld16(a.tmem + kTmemS + 128 + lane_off + 16 * c, s1);
+      ptx::tmem_ld16(a.tmem + kTmemS + 192 + lane_off + 16 * c, s2);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) s0[j] += s1[j] + s2[j];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float hi = __shfl_sync(0xffffffffu, s0[8 + j], lane & 15);
+        x[8 * c + j] = half ? hi : s0[j];
+      }
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&ms->s_empty);
+    const int key = a.kv_begin + t * kTileKeys + krow;
+    const int tile_last = a.kv_begin + t * kTileKeys + kTileKeys - 1;
+    const bool unmasked = tile_last < a.kv_end && tile_last < lim_min;  // tile-uniform fast path
+    bool need = false;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      const int n0 = 16 * c + 8 * half;
+      const float4 r0 = *reinterpret_cast<const float4*>(&ms->ref[n0]);
+      const float4 r1 = *reinterpret_cast<const float4*>(&ms->ref[n0 + 4]);
+      const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float v = x[8 * c + j] * scale;
+        if (!unmasked) v = (key < a.kv_end && key < ms->lim[n0 + j]) ? v : -INFINITY;
+        x[8 * c + j] = v;
+        need |= v > rr[j] + kRefSlack;
+      }
+    }
+    const unsigned vote = __any_sync(0xffffffffu, need);
+    if (lane == 0) ms->flags[sb][qd] = vote ? 1 : 0;
+    ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
+    if (!ok) break;
+    const bool moved = ms->flags[sb][0] | ms->flags[sb][1] | ms->flags[sb][2] | ms->flags[sb][3];
+    if (moved) {
+      // column maxima over this tile's keys (16 keys per half-warp), then move each
+      // row's reference up to its maximum
+#pragma unroll
+      for (int i = 0; i < NC; ++i) {
+        float m = x[i];
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((lane & 15) == 0) ms->colred[qd][16 * (i / 8) + 8 * half + (i % 8)] = m;
+      }
+      ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
+      if (!ok) break;
+      if (sidx < 16 * NCH) {
+        const float cm = fmaxf(fmaxf(ms->colred[0][sidx], ms->colred[1][sidx]), fmaxf(ms->colred[2][sidx], ms->colred[3][sidx]));
+        const float old = ms->ref[sidx];
+        const float nw = fmaxf(old, cm);
+        ms->alpha[sidx] = (nw == old) ? 1.f : ex2(old - nw);
+        ms->ref[sidx] = nw;
+      }
+      ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
+      if (!ok) break;
+#pragma unroll
+      for (int i = 0; i < NC; ++i) l_acc[i] *= ms->alpha[16 * (i / 8) + 8 * half + (i % 8)];
+      if (t >= 1) {
+        // O^T holds tiles < t: wait for PV(t-1), then scale each row's column by alpha
+        ok = warp_wait(&ms->pt_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, p.status);
+        if (!ok) break;
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            float o[16];
+            const uint32_t ta = a.tmem + kTmemO + 64 * blk + lane_off + 16 * c;
+            ptx::tmem_ld16(ta, o);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] *= ms->alpha[16 * c + j];
+            ptx::tmem_st16(ta, o);
+          }
+        }
+        ptx::tmem_st_wait();
+      }
+    }
+    // probabilities relative to the (possibly moved) reference, packed to bf16
+    uint32_t pk[NC / 2];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      const int n0 = 16 * c + 8 * half;
+      const float4 r0 = *reinterpret_cast<const float4*>(&ms->ref[n0]);
+      const float4 r1 = *reinterpret_cast<const float4*>(&ms->ref[n0 + 4]);
+      const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+        const float v0 = x[8 * c + j], v1 = x[8 * c + j + 1];
+        const float p0 = v0 == -INFINITY ? 0.f : ex2(v0 - rr[j]);
+        const float p1 = v1 == -INFINITY ? 0.f : ex2(v1 - rr[j + 1]);
+        l_acc[8 * c + j] += p0;
+        l_acc[8 * c + j + 1] += p1;
+        pk[(8 * c + j) / 2] = pack_bf16(p0, p1);
+      }
+    }
+    if (t >= 2) {
+      ok = warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p.status);
+      if (!ok) break;
+    }
+    uint8_t* line = a.sPt + sb * kPtBytes + krow * 128;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c)
+      *reinterpret_cast<uint4*>(line + ((((2 * c + half) ^ (krow & 7)) & 7) << 4)) =
+          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    if (key >= a.kv_end) {
+      // a cache slot past the key range: zero its value columns so P = 0 meets V = 0
+      uint8_t* row = a.sKv + sb * kSlotBytes + krow * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(row + (4 * half + c) * kKvChunkBytes + 16 * j) = make_uint4(0, 0, 0, 0);
+    }
+    ptx::fence_async_smem();
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&ms->p_full[sb]);
+  }
+  // ------------------------------------------------------------ epilogue
+  if (ok) ok = warp_wait(&ms->pt_empty[(a.ntiles - 1) & 1], ((a.ntiles - 1) >> 1) & 1, abort, p.status);
+  if (ok) {
+    ptx::tc_fence_after();
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+      float s = l_acc[i];
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if ((lane & 15) == 0) ms->colred[qd][16 * (i / 8) + 8 * half + (i % 8)] = s;
+    }
+    ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
+  }
+  if (ok) {
+    if (sidx < a.nrows) {
+      const float L = ms->colred[0][sidx] + ms->colred[1][sidx] + ms->colred[2][sidx] + ms->colred[3][sidx];
+      ms->lsum[sidx] = L;
+      const float lse_v = L > 0.f ? (ms->ref[sidx] + lg2(L)) * 0.69314718055994531f : -INFINITY;
+      if (a.part_row0 < 0) {
+        if (p.lse) p.lse[a.qrow0 + sidx] = lse_v;
+      } else {
+        p.part_lse[a.part_row0 + sidx] = lse_v;
+      }
+    }
+    ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
+  }
+  if (ok) {
+    const int dv_in_blk = qd * 32 + lane;
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+      const int dv = blk * 128 + dv_in_blk;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        float o[16];
+        ptx::tmem_ld16(a.tmem + kTmemO + 64 * blk + lane_off + 16 * c, o);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int n = 16 * c + j;
+          if (n < a.nrows) {
+            const float L = ms->lsum[n];
+            const float v = L > 0.f ? o[j] * (p.out_scale / L) : 0.f;
+            if (a.part_row0 < 0)
+              p.out[(size_t)(a.qrow0 + n) * kDv + dv] = __float2bfloat16_rn(v);
+            else
+              p.part_o[(size_t)(a.part_row0 + n) * kDv + dv] = v;
+          }
+        }
+      }
+    }
+  }
+}
+
 template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     fold_decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv, Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned base (the 128-byte swizzle atoms), kept in the shared window
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
   Misc* ms = (Misc*)(smem + kOffMisc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort = &ms->abort;
@@ -308,86 +564,112 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t gphase = 0;
     bool ok = !*abort && warp_wait(&ms->bar_q, 0, abort, p.status);
     bool issued_any = false;
-    for (int t = 0; ok && t <= ntiles; ++t) {
-      if (t < ntiles) {
-        const int slot = t & 1;
-        ok = warp_wait(&ms->kv_full[slot], (t >> 1) & 1, abort, p.status);
-        if (!ok) break;
-        if (kFp8) {
-          // this warp's chunks: read every e4m3 byte first (the bf16 rows overwrite the
-          // e4m3 staging area of other chunks), then write the bf16 rows
-          uint8_t* base = sKv + slot * kSlotBytes;
-          const int k = lane * 2;  // keys 2 lane, 2 lane + 1
-          uint4 raw[3][2][4];
-#pragma unroll
-          for (int ci = 0; ci < 3; ++ci)
-            if (c_lo + ci < c_hi)
-#pragma unroll
-              for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  raw[ci][kk][j] = *reinterpret_cast<const uint4*>(base + kFp8StageOff + (c_lo + ci) * kFp8ChunkBytes +
-                                                                   (k + kk) * 64 + 16 * j);
-          ok = group_sync(&ms->grp_mma, gphase, abort, p.status);
-          if (!ok) break;
-#pragma unroll
-          for (int ci = 0; ci < 3; ++ci)
-            if (c_lo + ci < c_hi)
-#pragma unroll
-              for (int kk = 0; kk < 2; ++kk) {
-                uint8_t* line = base + (c_lo + ci) * kKvChunkBytes + (k + kk) * 128;
-                const int sw = (k + kk) & 7;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  uint4 o0, o1;
-                  e4m3x4_to_bf16x4(raw[ci][kk][j].x, o0.x, o0.y);
-                  e4m3x4_to_bf16x4(raw[ci][kk][j].y, o0.z, o0.w);
-                  e4m3x4_to_bf16x4(raw[ci][kk][j].z, o1.x, o1.y);
-                  e4m3x4_to_bf16x4(raw[ci][kk][j].w, o1.z, o1.w);
-                  *reinterpret_cast<uint4*>(line + (((2 * j) ^ sw) << 4)) = o0;
-                  *reinterpret_cast<uint4*>(line + (((2 * j + 1) ^ sw) << 4)) = o1;
-                }
-              }
-          ptx::fence_async_smem();
-          __syncwarp();
-        }
-        if (t >= 1) {
-          ok = warp_wait(&ms->s_empty, (t - 1) & 1, abort, p.status);  // the softmax has read S(t-1)
-          if (!ok) break;
-        }
-        ptx::tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a0 = skv + slot * kSlotBytes;
-          for (int c = c_lo; c < c_hi; ++c) {
+    // Event loop: issue whichever product is ready, O^T first. S^T(t1) needs page t1 and
+    // the softmax's read of S^T(t1-1); O^T(t2) needs P^T(t2). O^T(t2) must not wait for
+    // page t2+1, or the slot of page t2 (and so the load of page t2+2) would be held back.
+    int t1 = 0, t2 = 0;
+    long long idle_t0 = clock64();
+    while (ok && t2 < ntiles) {
+      bool progressed = false;
+      if (t2 < t1) {
+        int rdy = 0;
+        if (lane == 0) rdy = ptx::mbar_test_wait(&ms->p_full[t2 & 1], (t2 >> 1) & 1);
+        if (__shfl_sync(0xffffffffu, rdy, 0)) {
+          const int ub = t2 & 1;
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t v0 = skv + ub * kSlotBytes + 2 * pw * kKvChunkBytes, pt0 = spt + ub * kPtBytes;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
+              uint64_t ad = ptx::smem_desc(v0 + 2048 * k, kKvChunkBytes, 1024, ptx::kSwizzle128B);
+              uint64_t bd = ptx::smem_desc(pt0 + 2048 * k, 8192, 1024, ptx::kSwizzle128B);
+              ptx::mma_bf16_ss(d_o, ad, bd, idesc_o, (t2 > 0 || k > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(&ms->kv_empty[ub]);
+            ptx::mma_commit(&ms->pt_empty[ub]);
+          }
+          __syncwarp();
+          ++t2;
+          progressed = true;
+        }
+      }
+      if (t1 < ntiles && t1 <= t2 + 1) {
+        int rdy = 0;
+        if (lane == 0)
+          rdy = ptx::mbar_test_wait(&ms->kv_full[t1 & 1], (t1 >> 1) & 1) &&
+                (t1 == 0 || ptx::mbar_test_wait(&ms->s_empty, (t1 - 1) & 1));
+        if (__shfl_sync(0xffffffffu, rdy, 0)) {
+          const int slot = t1 & 1;
+          if (kFp8) {
+            // this warp's chunks: read every e4m3 byte first (the bf16 rows overwrite the
+            // e4m3 staging area of other chunks), then write the bf16 rows. Lane l reads the
+            // 16-byte pieces l, l+32, ... of a chunk (conflict-free): key 8i + l/4, columns
+            // 16 (l%4) .. 16 (l%4) + 15.
+            uint8_t* base = sKv + slot * kSlotBytes;
+            uint4 raw[3][8];
+#pragma unroll
+            for (int ci = 0; ci < 3; ++ci)
+              if (c_lo + ci < c_hi)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  raw[ci][i] = *reinterpret_cast<const uint4*>(base + kFp8StageOff + (c_lo + ci) * kFp8ChunkBytes +
+                                                               i * 512 + 16 * lane);
+            ok = group_sync(&ms->grp_mma, gphase, abort, p.status);
+            if (!ok) break;
+            const int j = lane & 3;
+#pragma unroll
+            for (int ci = 0; ci < 3; ++ci)
+              if (c_lo + ci < c_hi)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const int key = 8 * i + (lane >> 2);
+                  uint8_t* line = base + (c_lo + ci) * kKvChunkBytes + key * 128;
+                  uint4 o0, o1;
+                  e4m3x4_to_bf16x4(raw[ci][i].x, o0.x, o0.y);
+                  e4m3x4_to_bf16x4(raw[ci][i].y, o0.z, o0.w);
+                  e4m3x4_to_bf16x4(raw[ci][i].z, o1.x, o1.y);
+                  e4m3x4_to_bf16x4(raw[ci][i].w, o1.z, o1.w);
+                  *reinterpret_cast<uint4*>(line + (((2 * j) ^ (key & 7)) << 4)) = o0;
+                  *reinterpret_cast<uint4*>(line + (((2 * j + 1) ^ (key & 7)) << 4)) = o1;
+                }
+            ptx::fence_async_smem();
+            // the K-steps of this warp's S^T MMAs span chunks expanded by other warps
+            ok = group_sync(&ms->grp_mma, gphase, abort, p.status);
+            if (!ok) break;
+          }
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = skv + slot * kSlotBytes;
+#pragma unroll
+            for (int i = 0; i < kKStepsPerWarp; ++i) {
+              const int ks = kKStepsPerWarp * pw + i, c = ks >> 2, k = ks & 3;
               uint64_t ad = ptx::smem_desc(a0 + c * kKvChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
               uint64_t bd = ptx::smem_desc(sq + c * kQChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
-              ptx::mma_bf16_ss(d_s, ad, bd, idesc_s, (c != c_lo || k != 0) ? 1u : 0u);
+              ptx::mma_bf16_ss(d_s, ad, bd, idesc_s, i != 0 ? 1u : 0u);
             }
+            ptx::mma_commit(&ms->s_full);
           }
-          ptx::mma_commit(&ms->s_full);
+          __syncwarp();
+          issued_any = true;
+          ++t1;
+          progressed = true;
         }
-        issued_any = true;
-        __syncwarp();
       }
-      if (t >= 1) {
-        const int u = t - 1, ub = u & 1;
-        ok = warp_wait(&ms->p_full[ub], (u >> 1) & 1, abort, p.status);
-        if (!ok) break;
-        ptx::tc_fence_after();
+      if (progressed) {
+        idle_t0 = clock64();
+      } else {
+        __nanosleep(32);  // leave issue slots to the softmax warps on this SM sub-partition
+        int stop = 0;
         if (lane == 0) {
-          const uint32_t v0 = skv + ub * kSlotBytes + 2 * pw * kKvChunkBytes, pt0 = spt + ub * kPtBytes;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint64_t ad = ptx::smem_desc(v0 + 2048 * k, kKvChunkBytes, 1024, ptx::kSwizzle128B);
-            uint64_t bd = ptx::smem_desc(pt0 + 2048 * k, 8192, 1024, ptx::kSwizzle128B);
-            ptx::mma_bf16_ss(d_o, ad, bd, idesc_o, (u > 0 || k > 0) ? 1u : 0u);
+          if (*abort) {
+            stop = 1;
+          } else if (clock64() - idle_t0 > kWaitBudget) {
+            *abort = 1;
+            report(p.status, MLA_DEVICE_WAIT_TIMEOUT);
+            stop = 1;
           }
-          ptx::mma_commit(&ms->kv_empty[ub]);
-          ptx::mma_commit(&ms->pt_empty[ub]);
         }
-        __syncwarp();
+        if (__shfl_sync(0xffffffffu, stop, 0)) ok = false;
       }
     }
     // every MMA this warp issued must retire before TMEM is released
@@ -403,203 +685,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int qd = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int sidx = tid - 32 * (kMmaWarps + 1);   // 0..127
-    const int krow = m64_row_of_lane(qd, lane);
-    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
-    uint32_t gphase = 0;
-    if (sidx < 64) {
-      int lim = 0;
-      if (sidx < nrows) {
-        const int i = (qrow0 + sidx) / p.H - tok0;  // verify token of this packed row
-        lim = ctx - qlen + i + 1;
-      }
-      ms->lim[sidx] = lim;
-      ms->ref[sidx] = -INFINITY;
-    }
-    bool ok = group_sync(&ms->grp_softmax, gphase, abort, p.status) && !*abort;
-    float l_acc[kRowsCap];
-#pragma unroll
-    for (int n = 0; n < kRowsCap; ++n) l_acc[n] = 0.f;
-    for (int t = 0; ok && t < ntiles; ++t) {
-      const int sb = t & 1;
-      ok = warp_wait(&ms->s_full, t & 1, abort, p.status);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      // S^T = sum of the four partial accumulators
-      float x[kRowsCap];
-#pragma unroll
-      for (int c = 0; c < kRowsCap / 16; ++c) {
-        if (c < nch) {
-          float y[2][16];
-          ptx::tmem_ld16(tmem + kTmemS + lane_off + 16 * c, x + 16 * c);
-          ptx::tmem_ld16(tmem + kTmemS + 64 + lane_off + 16 * c, y[0]);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) x[16 * c + j] += y[0][j];
-          ptx::tmem_ld16(tmem + kTmemS + 128 + lane_off + 16 * c, y[0]);
-          ptx::tmem_ld16(tmem + kTmemS + 192 + lane_off + 16 * c, y[1]);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) x[16 * c + j] += y[0][j] + y[1][j];
-        }
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&ms->s_empty);
-      const int key = kv_begin + t * kTileKeys + krow;
-      const bool valid = krow >= 0 && key < kv_end;
-      bool need = false;
-#pragma unroll
-      for (int n = 0; n < kRowsCap; ++n) {
-        if (n < nmma) {
-          const float v = (valid && key < ms->lim[n]) ? x[n] * p.score_scale_log2 : -INFINITY;
-          x[n] = v;
-          need |= v > ms->ref[n] + kRefSlack;
-        }
-      }
-      const unsigned vote = __any_sync(0xffffffffu, need);
-      if (lane == 0) ms->flags[sb][qd] = vote ? 1 : 0;
-      ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
-      if (!ok) break;
-      const bool moved = ms->flags[sb][0] | ms->flags[sb][1] | ms->flags[sb][2] | ms->flags[sb][3];
-      if (moved) {
-        // column maxima over this tile's keys, then move each row's reference up to it
-#pragma unroll
-        for (int n = 0; n < kRowsCap; ++n) {
-          if (n < nmma) {
-            float m = x[n];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0) ms->colred[qd][n] = m;
-          }
-        }
-        ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
-        if (!ok) break;
-        if (sidx < nmma) {
-          const float cm = fmaxf(fmaxf(ms->colred[0][sidx], ms->colred[1][sidx]), fmaxf(ms->colred[2][sidx], ms->colred[3][sidx]));
-          const float old = ms->ref[sidx];
-          const float nw = fmaxf(old, cm);
-          ms->alpha[sidx] = (nw == old) ? 1.f : ex2(old - nw);
-          ms->ref[sidx] = nw;
-        }
-        ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
-        if (!ok) break;
-#pragma unroll
-        for (int n = 0; n < kRowsCap; ++n)
-          if (n < nmma) l_acc[n] *= ms->alpha[n];
-        if (t >= 1) {
-          // O^T holds tiles < t: wait for PV(t-1), then scale each row's column by alpha
-          ok = warp_wait(&ms->pt_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, p.status);
-          if (!ok) break;
-          ptx::tc_fence_after();
-#pragma unroll 1
-          for (int blk = 0; blk < 4; ++blk) {
-#pragma unroll 1
-            for (int c = 0; c < nch; ++c) {
-              float o[16];
-              const uint32_t ta = tmem + kTmemO + 64 * blk + lane_off + 16 * c;
-              ptx::tmem_ld16(ta, o);
-              ptx::tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < 16; ++j) o[j] *= ms->alpha[16 * c + j];
-              ptx::tmem_st16(ta, o);
-            }
-          }
-          ptx::tmem_st_wait();
-        }
-      }
-      // probabilities relative to the (possibly moved) reference
-      uint32_t pk[kRowsCap / 2];
-#pragma unroll
-      for (int n = 0; n < kRowsCap; n += 2) {
-        float p0 = 0.f, p1 = 0.f;
-        if (n < nmma) {
-          p0 = x[n] == -INFINITY ? 0.f : ex2(x[n] - ms->ref[n]);
-          p1 = x[n + 1] == -INFINITY ? 0.f : ex2(x[n + 1] - ms->ref[n + 1]);
-          l_acc[n] += p0;
-          l_acc[n + 1] += p1;
-        }
-        pk[n / 2] = pack_bf16(p0, p1);
-      }
-      if (t >= 2) {
-        ok = warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p.status);
-        if (!ok) break;
-      }
-      if (krow >= 0) {
-        uint8_t* line = sPt + sb * kPtBytes + krow * 128;
-#pragma unroll
-        for (int j = 0; j < kRowsCap / 8; ++j)
-          if (j < nmma / 8)
-            *reinterpret_cast<uint4*>(line + (((j ^ (krow & 7)) & 7) << 4)) =
-                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        if (key >= kv_end) {
-          // a cache slot past the key range: zero its value columns so P = 0 meets V = 0
-          uint8_t* slot = sKv + sb * kSlotBytes + krow * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(slot + c * kKvChunkBytes + 16 * j) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      ptx::fence_async_smem();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&ms->p_full[sb]);
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok) ok = warp_wait(&ms->pt_empty[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort, p.status);
-    if (ok) {
-      ptx::tc_fence_after();
-#pragma unroll
-      for (int n = 0; n < kRowsCap; ++n) {
-        if (n < nmma) {
-          float s = l_acc[n];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-          if (lane == 0) ms->colred[qd][n] = s;
-        }
-      }
-      ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
-    }
-    if (ok) {
-      if (sidx < nrows) {
-        const float L = ms->colred[0][sidx] + ms->colred[1][sidx] + ms->colred[2][sidx] + ms->colred[3][sidx];
-        ms->lsum[sidx] = L;
-        const float lse_v = L > 0.f ? (ms->ref[sidx] + lg2(L)) * 0.69314718055994531f : -INFINITY;
-        if (part_row0 < 0) {
-          if (p.lse) p.lse[qrow0 + sidx] = lse_v;
-        } else {
-          p.part_lse[part_row0 + sidx] = lse_v;
-        }
-      }
-      ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
-    }
-    if (ok) {
-      const int dv_in_blk = qd * 32 + lane;
-#pragma unroll 1
-      for (int blk = 0; blk < 4; ++blk) {
-        const int dv = blk * 128 + dv_in_blk;
-#pragma unroll 1
-        for (int c = 0; c < nch; ++c) {
-          float o[16];
-          ptx::tmem_ld16(tmem + kTmemO + 64 * blk + lane_off + 16 * c, o);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int n = 16 * c + j;
-            if (n < nrows) {
-              const float L = ms->lsum[n];
-              const float v = L > 0.f ? o[j] * (p.out_scale / L) : 0.f;
-              if (part_row0 < 0)
-                p.out[(size_t)(qrow0 + n) * kDv + dv] = __float2bfloat16_rn(v);
-              else
-                p.part_o[(size_t)(part_row0 + n) * kDv + dv] = v;
-            }
-          }
-        }
-      }
-    }
+    const SoftmaxArgs a{ms, sKv, sPt, tmem, warp & 3, lane, tid - 32 * (kMmaWarps + 1), nrows, qrow0, kv_begin, kv_end,
+                        ntiles, part_row0, ctx, qlen, tok0, abort};
+    if (nch == 1)
+      softmax_role<1>(a, p);
+    else if (nch == 2)
+      softmax_role<2>(a, p);
+    else
+      softmax_role<3>(a, p);
   }
 
   ptx::tc_fence_before();
