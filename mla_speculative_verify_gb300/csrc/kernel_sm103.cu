@@ -179,9 +179,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 // e4m3 x4 (one 32-bit word) -> bf16 x4 (two 32-bit words), exact, through the
-// hardware conversions (used for words that hold a zero, subnormal or NaN code). Kept
-// out of line so that the common path below stays a branch, not a predicated copy.
-__device__ __noinline__ void e4m3x4_to_bf16x4_cvt(uint32_t w, uint32_t& lo, uint32_t& hi) {
+// hardware conversions (for pages that hold a zero, subnormal or NaN code).
+__device__ __forceinline__ void e4m3x4_to_bf16x4_cvt(uint32_t w, uint32_t& lo, uint32_t& hi) {
   __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
   __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
   float2 f0 = __half22float2(*reinterpret_cast<__half2*>(&h0));
@@ -190,24 +189,24 @@ __device__ __noinline__ void e4m3x4_to_bf16x4_cvt(uint32_t w, uint32_t& lo, uint
   hi = pack_bf16(f1.x, f1.y);
 }
 
-// e4m3 x4 -> bf16 x4 with integer operations. A normal e4m3 code s.eeee.mmm equals
-// (-1)^s 2^(e-7) (1 + m/8); the bf16 with exponent field e + 120 and mantissa m << 4 holds
-// the same value, so each 16-bit half is ((c & 0x7F) << 4) + (120 << 7) with the sign
-// moved to bit 15. Codes with e = 0 (zero, subnormals) and the NaN codes S.1111.111
-// take the conversion path.
-__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t ex = w & 0x78787878u;                  // zero byte <=> zero exponent
-  const uint32_t nn = (w & 0x7F7F7F7Fu) ^ 0x7F7F7F7Fu;  // zero byte <=> NaN code
-  if ((((ex - 0x01010101u) & ~ex) | ((nn - 0x01010101u) & ~nn)) & 0x80808080u) {
-    e4m3x4_to_bf16x4_cvt(w, lo, hi);
-    return;
-  }
+// e4m3 x4 -> bf16 x4 with integer operations, exact for normal codes. A normal e4m3
+// code s.eeee.mmm equals (-1)^s 2^(e-7) (1 + m/8); the bf16 with exponent field e + 120
+// and mantissa m << 4 holds the same value, so each 16-bit half is
+// ((c & 0x7F) << 4) + (120 << 7) with the sign moved to bit 15.
+__device__ __forceinline__ void e4m3x4_to_bf16x4_normal(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t a = __byte_perm(w, 0u, 0x4140);  // codes 0, 1 in the low bytes of the halves
   const uint32_t b = __byte_perm(w, 0u, 0x4342);  // codes 2, 3
   lo = (((a & 0x007F007Fu) << 4) + 0x3C003C00u) | ((a & 0x00800080u) << 8);
   hi = (((b & 0x007F007Fu) << 4) + 0x3C003C00u) | ((b & 0x00800080u) << 8);
 }
 
+// Nonzero when one of the four codes is zero/subnormal (exponent 0) or NaN (S.1111.111):
+// those need the exact conversion.
+__device__ __forceinline__ uint32_t e4m3x4_special(uint32_t w) {
+  const uint32_t ex = w & 0x78787878u;                  // zero byte <=> zero exponent
+  const uint32_t nn = (w & 0x7F7F7F7Fu) ^ 0x7F7F7F7Fu;  // zero byte <=> NaN code
+  return (((ex - 0x01010101u) & ~ex) | ((nn - 0x01010101u) & ~nn)) & 0x80808080u;
+}
 
 struct SoftmaxArgs {
   Misc* ms;
@@ -617,21 +616,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = group_sync(&ms->grp_mma, gphase, abort, p.status);
             if (!ok) break;
             const int j = lane & 3;
+            // one warp-uniform decision per page: integer expansion unless this warp's share
+            // holds a code that needs the exact conversion (zero, subnormal, NaN)
+            uint32_t special = 0;
 #pragma unroll
             for (int ci = 0; ci < 3; ++ci)
               if (c_lo + ci < c_hi)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const int key = 8 * i + (lane >> 2);
-                  uint8_t* line = base + (c_lo + ci) * kKvChunkBytes + key * 128;
-                  uint4 o0, o1;
-                  e4m3x4_to_bf16x4(raw[ci][i].x, o0.x, o0.y);
-                  e4m3x4_to_bf16x4(raw[ci][i].y, o0.z, o0.w);
-                  e4m3x4_to_bf16x4(raw[ci][i].z, o1.x, o1.y);
-                  e4m3x4_to_bf16x4(raw[ci][i].w, o1.z, o1.w);
-                  *reinterpret_cast<uint4*>(line + (((2 * j) ^ (key & 7)) << 4)) = o0;
-                  *reinterpret_cast<uint4*>(line + (((2 * j + 1) ^ (key & 7)) << 4)) = o1;
-                }
+                for (int i = 0; i < 8; ++i)
+                  special |= e4m3x4_special(raw[ci][i].x) | e4m3x4_special(raw[ci][i].y) |
+                             e4m3x4_special(raw[ci][i].z) | e4m3x4_special(raw[ci][i].w);
+            if (!__any_sync(0xffffffffu, special != 0u)) {
+#pragma unroll
+              for (int ci = 0; ci < 3; ++ci)
+                if (c_lo + ci < c_hi)
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) {
+                    const int key = 8 * i + (lane >> 2);
+                    uint8_t* line = base + (c_lo + ci) * kKvChunkBytes + key * 128;
+                    uint4 o0, o1;
+                    e4m3x4_to_bf16x4_normal(raw[ci][i].x, o0.x, o0.y);
+                    e4m3x4_to_bf16x4_normal(raw[ci][i].y, o0.z, o0.w);
+                    e4m3x4_to_bf16x4_normal(raw[ci][i].z, o1.x, o1.y);
+                    e4m3x4_to_bf16x4_normal(raw[ci][i].w, o1.z, o1.w);
+                    *reinterpret_cast<uint4*>(line + (((2 * j) ^ (key & 7)) << 4)) = o0;
+                    *reinterpret_cast<uint4*>(line + (((2 * j + 1) ^ (key & 7)) << 4)) = o1;
+                  }
+            } else {
+#pragma unroll
+              for (int ci = 0; ci < 3; ++ci)
+                if (c_lo + ci < c_hi)
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) {
+                    const int key = 8 * i + (lane >> 2);
+                    uint8_t* line = base + (c_lo + ci) * kKvChunkBytes + key * 128;
+                    uint4 o0, o1;
+                    e4m3x4_to_bf16x4_cvt(raw[ci][i].x, o0.x, o0.y);
+                    e4m3x4_to_bf16x4_cvt(raw[ci][i].y, o0.z, o0.w);
+                    e4m3x4_to_bf16x4_cvt(raw[ci][i].z, o1.x, o1.y);
+                    e4m3x4_to_bf16x4_cvt(raw[ci][i].w, o1.z, o1.w);
+                    *reinterpret_cast<uint4*>(line + (((2 * j) ^ (key & 7)) << 4)) = o0;
+                    *reinterpret_cast<uint4*>(line + (((2 * j + 1) ^ (key & 7)) << 4)) = o1;
+                  }
+            }
             ptx::fence_async_smem();
             // the K-steps of this warp's S^T MMAs span chunks expanded by other warps
             ok = group_sync(&ms->grp_mma, gphase, abort, p.status);

@@ -55,6 +55,19 @@ def test_edge_shapes(seq, q, H):
         _check(inputs.make_problem(H, seq, q, kv, seed=2300 + seq[0], poison_tail=True))
 
 
+def test_fp8_zero_and_subnormal_codes():
+    """Zero (both signs) and subnormal e4m3 codes in visible keys take the exact
+    expansion path; the rest of the page takes the integer path."""
+    prob = inputs.make_problem(12, [64 * 5 + 9], [4], FP8, seed=2450)
+    g = torch.Generator().manual_seed(3)
+    rows = prob.kv.shape[0]
+    idx = torch.randint(0, rows * 576, (4000,), generator=g)
+    codes = torch.tensor([0x00, 0x80, 0x01, 0x87, 0x05, 0x83], dtype=torch.uint8)
+    prob.kv.view(-1)[idx] = codes[torch.randint(0, len(codes), (4000,), generator=g)]
+    prob.kv[64:128] = 0  # one whole page of zero codes
+    _check(prob)
+
+
 def test_many_splits_with_empty_causal_partials():
     """One page per split: the last split holds keys that early verify rows may not see."""
     prob = inputs.make_problem(12, [64 * 6 + 3], [8], BF16, seed=2400, poison_tail=True)
