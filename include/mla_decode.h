@@ -31,7 +31,8 @@
  *
  * Ownership: the caller owns and allocates every buffer. The library allocates
  * no memory, never synchronises the stream, and keeps no state between calls
- * apart from a thread-local error string.
+ * apart from a thread-local error string (and the fixed device array behind
+ * mla_decode_run_static_ws, declared below).
  *
  * Errors: every entry point returns an mla_status; on failure mla_last_error()
  * describes the cause. Arguments are checked on the host before any launch.
@@ -145,6 +146,35 @@ int mla_decode_run(const void* plan_dev, const void* plan_host, size_t plan_byte
                    int num_pages, const int32_t* seq_lens, const int32_t* q_lens, float sm_scale,
                    float kv_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
                    int32_t* status_dev, void* stream);
+
+/*
+ * mla_decode_run_static_ws -- mla_decode_run without a caller-supplied workspace.
+ *
+ * The pages have no counterpart for this entry point; it exists for callers that
+ * cannot allocate device memory: code running where an allocation would synchronise
+ * the device or break a real-time budget, plug-in hosts that hand out only the
+ * input and output buffers and own every allocator, and runtimes with a fixed memory
+ * plan. The split-KV partials go to a library-owned device array of
+ * MLA_STATIC_WORKSPACE_BYTES (16 MiB), which every GPU that loads the library holds
+ * until the process exits. The call itself allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).
+ *
+ *   Arguments are those of mla_decode_run without workspace / workspace_bytes.
+ *   A plan whose workspace exceeds the array (mla_decode_plan reports the size) is
+ *   rejected with MLA_ERR_BUFFER before any launch; plan with fewer splits
+ *   (mla_plan_options.force_splits) or use mla_decode_run with your own workspace.
+ *   The first call on a device looks up the array's device address (once, with that
+ *   device current); make that first call before any stream capture.
+ *   Every call in the process shares the one array per device and overwrites what the
+ *   previous call left in it; nothing in it needs clearing. Calls whose kernels
+ *   overlap on the GPU (for example on two concurrent streams) race on the array, so
+ *   serialise them.
+ */
+#define MLA_STATIC_WORKSPACE_BYTES (16u << 20)
+int mla_decode_run_static_ws(const void* plan_dev, const void* plan_host, size_t plan_bytes, const void* q,
+                             const void* kv_cache, const int32_t* page_table, int page_table_stride, int num_pages,
+                             const int32_t* seq_lens, const int32_t* q_lens, float sm_scale, float kv_scale, void* out,
+                             float* lse, int32_t* status_dev, void* stream);
 
 /* Message of the last failed call on this thread ("" if none). */
 const char* mla_last_error(void);

@@ -25,6 +25,7 @@ MLA_KV_FP8_E4M3 = 1
 MLA_DEVICE_WAIT_TIMEOUT = 0x1
 MLA_DEVICE_PLAN_MISMATCH = 0x2
 MLA_DEVICE_BAD_PAGE = 0x4
+MLA_STATIC_WORKSPACE_BYTES = 16 << 20
 
 _P = ctypes.c_void_p
 _I32P = ctypes.POINTER(ctypes.c_int32)
@@ -53,6 +54,8 @@ SIGNATURES = {
     "mla_decode_plan_info": (ctypes.c_int, [_P, ctypes.c_size_t, _IP, _IP, _IP, _IP, _IP]),
     "mla_decode_run": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P, _P, _P, ctypes.c_int, ctypes.c_int, _P, _P,
                                       ctypes.c_float, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "mla_decode_run_static_ws": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P, _P, _P, ctypes.c_int, ctypes.c_int, _P,
+                                                 _P, ctypes.c_float, ctypes.c_float, _P, _P, _P, _P]),
     "mla_last_error": (ctypes.c_char_p, []),
     "mla_version": (ctypes.c_int, []),
 }
@@ -137,6 +140,19 @@ def run(plan_dev_ptr: int, plan_host: np.ndarray, q_ptr: int, kv_ptr: int, page_
                             page_table_ptr, int(page_table_stride), int(num_pages), seq_lens_ptr, q_lens_ptr,
                             float(sm_scale), float(kv_scale), out_ptr, lse_ptr, workspace_ptr, int(workspace_bytes),
                             status_ptr, stream_handle)
+    check(rc, lib)
+
+
+def run_static_ws(plan_dev_ptr: int, plan_host: np.ndarray, q_ptr: int, kv_ptr: int, page_table_ptr: int,
+                  page_table_stride: int, num_pages: int, seq_lens_ptr: int, q_lens_ptr: int, sm_scale: float,
+                  kv_scale: float, out_ptr: int, lse_ptr: int | None, status_ptr: int | None,
+                  stream_handle: int) -> None:
+    """mla_decode_run_static_ws: the decode with the library's own split-KV scratch."""
+    lib = load()
+    rc = lib.mla_decode_run_static_ws(plan_dev_ptr, plan_host.ctypes.data_as(_P), plan_host.nbytes, q_ptr, kv_ptr,
+                                      page_table_ptr, int(page_table_stride), int(num_pages), seq_lens_ptr,
+                                      q_lens_ptr, float(sm_scale), float(kv_scale), out_ptr, lse_ptr, status_ptr,
+                                      stream_handle)
     check(rc, lib)
 
 
