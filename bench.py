@@ -73,6 +73,24 @@ def algorithmic_flops(prob) -> float:
     return f
 
 
+def profiled_traffic(kernel_src: str, profile_md: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when the kernel source
+    changed since the counters were taken (the summary records the source hash)."""
+    import hashlib
+    import re
+
+    try:
+        text = open(profile_md).read()
+        sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != sha:
+        return None
+    return int(m_tr.group(1))
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -345,7 +363,13 @@ def main():
                           f"{sum(c['prob'].kv.numel() * c['prob'].kv.element_size() for c in res['calls']) / 1e6:.0f} MB in total > 126 MB L2"),
                    "timing": "CUDA-graph replay, CUDA events per call, median over steps", "per_call": rows},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "frac": round(achieved / hbm_peak, 4),
+                     "traffic": (profiled_traffic(os.path.join(ROOT, "mla_speculative_verify_gb300", "csrc",
+                                                               "kernel_sm103.cu"),
+                                                  os.path.join(ROOT, "profiles",
+                                                               "fold_decode_kernel_h12_q8_ctx131072_bf16.md"))
+                                 if dprob.name == "h12_q8_ctx131072_bf16" else None),
+                     "algorithmic_bytes": dbytes,
                      "kernel": f"fold_decode_kernel + lse_merge_kernel ({dprob.name})",
                      "peak_source": f"{peak_src} hbm_gbs"},
         "clocks": res["clocks"],
