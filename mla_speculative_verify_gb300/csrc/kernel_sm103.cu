@@ -57,19 +57,30 @@ constexpr int kTileKeys = 64;                      // keys per stage = one page
 constexpr int kChunks = 9;                         // 576 = 9 x 64 columns (128-byte swizzle rows)
 constexpr int kQChunkBytes = kRowsCap * 128;       // 6144
 constexpr int kQBytes = kChunks * kQChunkBytes;    // 55296
-constexpr int kKvChunkBytes = kTileKeys * 128;     // 8192
+constexpr int kKvChunkBytes = kTileKeys * 128;     // 8192 (bf16 page chunk: 64 keys x 64 columns)
 constexpr int kSlotBytes = kChunks * kKvChunkBytes;  // 73728 (bf16 page)
-constexpr int kFp8StageOff = kSlotBytes / 2;       // an e4m3 page lands in the upper half of its slot
-constexpr int kFp8ChunkBytes = kTileKeys * 64;     // 4096
-constexpr int kPtBytes = kTileKeys * 128;          // P^T tile: 64 keys x (<= 64 rows) bf16
+constexpr int kKvBytes = 2 * kSlotBytes;           // page ring: two bf16 stages or four e4m3 stages
+constexpr int kPtBytes = kTileKeys * 128;          // P^T tile: 64 keys x (<= 64 rows) bf16, or e4m3 hi + lo
 constexpr int kOffQ = 0;
 constexpr int kOffKv = kOffQ + kQBytes;
-constexpr int kOffPt = kOffKv + 2 * kSlotBytes;
+constexpr int kOffPt = kOffKv + kKvBytes;
 constexpr int kOffMisc = kOffPt + 2 * kPtBytes;
 constexpr int kMiscBytes = 4096;
 constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory");
 static_assert(kOffKv % 1024 == 0 && kOffPt % 1024 == 0 && kOffMisc % 1024 == 0, "1024-byte swizzle atoms");
+
+// Per cache dtype: a bf16 page is 128-byte rows per 64-column chunk (128-byte swizzle), an
+// e4m3 page 64-byte rows (64-byte swizzle), so the same ring holds two or four pages.
+template <bool kFp8>
+struct Geo {
+  static constexpr int kStages = kFp8 ? 4 : 2;
+  static constexpr int kRowBytes = kFp8 ? 64 : 128;           // bytes of one key in one chunk
+  static constexpr int kChunkBytes = kTileKeys * kRowBytes;   // 4096 / 8192
+  static constexpr int kSlot = kChunks * kChunkBytes;         // 36864 / 73728
+  static constexpr int kQPartBytes = kChunks * kRowsCap * 64; // e4m3 Q hi or lo part: 27648
+  static_assert(kStages * kSlot == kKvBytes, "ring size");
+};
 
 constexpr int kMmaWarps = 4;
 constexpr int kThreads = 32 * (1 + kMmaWarps + 4);  // producer, MMA warps, softmax warps
@@ -77,6 +88,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;       // O^T block b at columns 64 b (N <= 64)
 constexpr uint32_t kTmemS = 256;     // partial S^T p at columns 256 + 64 p
 constexpr float kRefSlack = 8.0f;    // octaves a score may exceed the row reference before it moves
+// e4m3 path: a smaller slack (p <= 4) so that P can be stored times 2^6 (<= 256 < 448,
+// the largest e4m3) and small probabilities stay above e4m3's subnormal range
+constexpr float kRefSlackFp8 = 2.0f;
+constexpr float kPScaleFp8 = 64.0f;
+constexpr int kPrefetchPages = 4;    // pages brought into L2 ahead of the two shared-memory stages
 constexpr long long kWaitBudget = 2000000000LL;  // cycles (~1 s) before a wait gives up
 
 // K-steps (16 columns each) of the S^T product owned by MMA warp p: [9 p, 9 p + 9) of
@@ -92,6 +108,8 @@ __device__ __forceinline__ int m64_row_of_lane(int quadrant, int lane) { return 
 
 struct Params {
   const uint8_t* plan;
+  const __nv_bfloat16* q;  // the e4m3 path converts its Q tile from global memory
+  int q_rows;              // rows of q (sum q_lens * H)
   const int32_t* page_table;
   int pt_stride, num_pages, H;
   const int32_t* seq_lens;
@@ -107,7 +125,7 @@ struct Params {
 
 struct Misc {
   uint64_t bar_q;
-  uint64_t kv_full[2], kv_empty[2];
+  uint64_t kv_full[4], kv_empty[4];
   uint64_t s_full, s_empty;
   uint64_t p_full[2], pt_empty[2];
   uint64_t mma_done;
@@ -122,6 +140,7 @@ struct Misc {
   alignas(16) int lim[64];
   alignas(16) float colred[4][64];
   alignas(16) float lsum[64];
+  alignas(16) float colscale[64];  // e4m3 path: score scale of each row (its Q split scale folded in)
 };
 static_assert(offsetof(Misc, ref) % 16 == 0, "float4 reads of ref need 16-byte alignment");
 static_assert(sizeof(Misc) <= kMiscBytes, "misc block too small");
@@ -178,38 +197,24 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// e4m3 x4 (one 32-bit word) -> bf16 x4 (two 32-bit words), exact, through the
-// hardware conversions (for pages that hold a zero, subnormal or NaN code).
-__device__ __forceinline__ void e4m3x4_to_bf16x4_cvt(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
-  __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
-  float2 f0 = __half22float2(*reinterpret_cast<__half2*>(&h0));
-  float2 f1 = __half22float2(*reinterpret_cast<__half2*>(&h1));
-  lo = pack_bf16(f0.x, f0.y);
-  hi = pack_bf16(f1.x, f1.y);
+// An fp32 rounded to the precision of e4m3 (4 significant bits, round to nearest even),
+// still as fp32; exact for magnitudes in e4m3's normal range.
+__device__ __forceinline__ float round_to_e4m3_precision(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return __uint_as_float((u + 0x7FFFFu + ((u >> 20) & 1u)) & 0xFFF00000u);
 }
-
-// e4m3 x4 -> bf16 x4 with integer operations, exact for normal codes. A normal e4m3
-// code s.eeee.mmm equals (-1)^s 2^(e-7) (1 + m/8); the bf16 with exponent field e + 120
-// and mantissa m << 4 holds the same value, so each 16-bit half is
-// ((c & 0x7F) << 4) + (120 << 7) with the sign moved to bit 15.
-__device__ __forceinline__ void e4m3x4_to_bf16x4_normal(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t a = __byte_perm(w, 0u, 0x4140);  // codes 0, 1 in the low bytes of the halves
-  const uint32_t b = __byte_perm(w, 0u, 0x4342);  // codes 2, 3
-  lo = (((a & 0x007F007Fu) << 4) + 0x3C003C00u) | ((a & 0x00800080u) << 8);
-  hi = (((b & 0x007F007Fu) << 4) + 0x3C003C00u) | ((b & 0x00800080u) << 8);
+// Two fp32 -> two e4m3 codes (round to nearest even, saturating), first in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
-
-// Nonzero when one of the four codes is zero/subnormal (exponent 0) or NaN (S.1111.111):
-// those need the exact conversion.
-__device__ __forceinline__ uint32_t e4m3x4_special(uint32_t w) {
-  const uint32_t ex = w & 0x78787878u;                  // zero byte <=> zero exponent
-  const uint32_t nn = (w & 0x7F7F7F7Fu) ^ 0x7F7F7F7Fu;  // zero byte <=> NaN code
-  return (((ex - 0x01010101u) & ~ex) | ((nn - 0x01010101u) & ~nn)) & 0x80808080u;
+// Byte offset of (row, column) in a 64-byte-swizzled e4m3 region with 64-byte rows.
+__device__ __forceinline__ int sw64_offset(int row, int col) {
+  return row * 64 + ((((col >> 4) ^ (row >> 1)) & 3) << 4) + (col & 15);
 }
 
 struct SoftmaxArgs {
   Misc* ms;
+  uint8_t* sQ;
   uint8_t* sKv;
   uint8_t* sPt;
   uint32_t tmem;
@@ -221,9 +226,10 @@ struct SoftmaxArgs {
 // S^T row from TMEM (the M = 64 accumulator uses 16 lanes per quadrant) and hand the
 // upper 8 of every 16 columns to lanes 16..31, so each thread works on 8 NCH columns of
 // one key: columns 16 c + 8 half + j, c < NCH, j < 8.
-template <int NCH>
+template <int NCH, bool kFp8>
 __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params& p) {
   constexpr int NC = 8 * NCH;
+  using G = Geo<kFp8>;
   Misc* ms = a.ms;
   const int lane = a.lane, qd = a.qd, sidx = a.sidx;
   const int half = lane >> 4;
@@ -239,6 +245,52 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
     }
     ms->lim[sidx] = lim;
     ms->ref[sidx] = -INFINITY;
+  }
+  if constexpr (kFp8) {
+    // Q tile -> e4m3 hi + lo parts (64-byte swizzle, K-major) for the e4m3 S^T MMAs. Row r
+    // is scaled by 2^e_r so that its largest |q| lands in [128, 256); hi = q 2^e_r rounded to
+    // e4m3, lo = the remainder in e4m3: hi + lo reproduces the bf16 row to ~2^-17 of its
+    // largest entry. 2^-e_r goes into the row's score scale.
+    const float base = p.score_scale_log2;
+    uint8_t* q_hi = a.sQ;
+    uint8_t* q_lo = a.sQ + G::kQPartBytes;
+    for (int r = qd; r < 16 * NCH; r += 4) {
+      const int grow = a.qrow0 + r;
+      float v[18];
+      if (grow < p.q_rows) {
+        const __nv_bfloat162* src = reinterpret_cast<const __nv_bfloat162*>(p.q + (size_t)grow * kDqk + 18 * lane);
+#pragma unroll
+        for (int j = 0; j < 9; ++j) {
+          const float2 f = __bfloat1622float2(src[j]);
+          v[2 * j] = f.x;
+          v[2 * j + 1] = f.y;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 18; ++j) v[j] = 0.f;
+      }
+      float mx = 0.f;
+#pragma unroll
+      for (int j = 0; j < 18; ++j) mx = fmaxf(mx, fabsf(v[j]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      int e = 0;
+      if (mx > 0.f && mx < INFINITY) e = max(-100, min(100, 7 - ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127)));
+      const float sc = __uint_as_float((uint32_t)(e + 127) << 23);  // 2^e
+#pragma unroll
+      for (int j = 0; j < 18; j += 2) {
+        const float w0 = v[j] * sc, w1 = v[j + 1] * sc;
+        const float h0 = round_to_e4m3_precision(w0), h1 = round_to_e4m3_precision(w1);
+        const int col = 18 * lane + j;  // even: the pair stays in one 16-byte piece
+        const int off = (col >> 6) * (kRowsCap * 64) + sw64_offset(r, col & 63);
+        *reinterpret_cast<uint16_t*>(q_hi + off) = (uint16_t)e4m3x2(h0, h1);
+        *reinterpret_cast<uint16_t*>(q_lo + off) = (uint16_t)e4m3x2(w0 - h0, w1 - h1);
+      }
+      if (lane == 0) ms->colscale[r] = base * __uint_as_float((uint32_t)(127 - e) << 23);
+    }
+    ptx::fence_async_smem();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&ms->bar_q);
   }
   bool ok = group_sync(&ms->grp_softmax, gphase, abort, p.status) && !*abort;
   int lim_min = a.kv_end;
@@ -286,12 +338,21 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
       const float4 r0 = *reinterpret_cast<const float4*>(&ms->ref[n0]);
       const float4 r1 = *reinterpret_cast<const float4*>(&ms->ref[n0 + 4]);
       const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+      float cs[8];
+      if constexpr (kFp8) {
+        const float4 c0 = *reinterpret_cast<const float4*>(&ms->colscale[n0]);
+        const float4 c1 = *reinterpret_cast<const float4*>(&ms->colscale[n0 + 4]);
+        cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w; cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cs[j] = scale;
+      }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        float v = x[8 * c + j] * scale;
+        float v = x[8 * c + j] * cs[j];
         if (!unmasked) v = (key < a.kv_end && key < ms->lim[n0 + j]) ? v : -INFINITY;
         x[8 * c + j] = v;
-        need |= v > rr[j] + kRefSlack;
+        need |= v > rr[j] + (kFp8 ? kRefSlackFp8 : kRefSlack);
       }
     }
     const unsigned vote = __any_sync(0xffffffffu, need);
@@ -343,8 +404,10 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
         ptx::tmem_st_wait();
       }
     }
-    // probabilities relative to the (possibly moved) reference, packed to bf16
+    // probabilities relative to the (possibly moved) reference, packed to bf16, or for the
+    // e4m3 path times 2^6 and split into hi + lo e4m3 parts
     uint32_t pk[NC / 2];
+    uint32_t ph[NC / 4], pl[NC / 4];
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
       const int n0 = 16 * c + 8 * half;
@@ -358,26 +421,46 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
         const float p1 = v1 == -INFINITY ? 0.f : ex2(v1 - rr[j + 1]);
         l_acc[8 * c + j] += p0;
         l_acc[8 * c + j + 1] += p1;
-        pk[(8 * c + j) / 2] = pack_bf16(p0, p1);
+        if constexpr (kFp8) {
+          const float w0 = p0 * kPScaleFp8, w1 = p1 * kPScaleFp8;
+          const float h0 = round_to_e4m3_precision(w0), h1 = round_to_e4m3_precision(w1);
+          const uint32_t hc = e4m3x2(h0, h1), lc = e4m3x2(w0 - h0, w1 - h1);
+          const int k4 = (8 * c + j) / 4, sh = ((8 * c + j) % 4) * 8;
+          if (sh == 0) { ph[k4] = hc; pl[k4] = lc; } else { ph[k4] |= hc << 16; pl[k4] |= lc << 16; }
+        } else {
+          pk[(8 * c + j) / 2] = pack_bf16(p0, p1);
+        }
       }
     }
     if (t >= 2) {
       ok = warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p.status);
       if (!ok) break;
     }
-    uint8_t* line = a.sPt + sb * kPtBytes + krow * 128;
+    if constexpr (kFp8) {
+      // e4m3 P^T hi and lo, MN-major with 64-byte rows (64-byte swizzle): key krow's row
+      uint8_t* line_hi = a.sPt + sb * kPtBytes + krow * 64;
+      uint8_t* line_lo = line_hi + kTileKeys * 64;
 #pragma unroll
-    for (int c = 0; c < NCH; ++c)
-      *reinterpret_cast<uint4*>(line + ((((2 * c + half) ^ (krow & 7)) & 7) << 4)) =
-          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      for (int c = 0; c < NCH; ++c) {
+        const int off = (((c ^ (krow >> 1)) & 3) << 4) + 8 * half;
+        *reinterpret_cast<uint2*>(line_hi + off) = make_uint2(ph[2 * c], ph[2 * c + 1]);
+        *reinterpret_cast<uint2*>(line_lo + off) = make_uint2(pl[2 * c], pl[2 * c + 1]);
+      }
+    } else {
+      uint8_t* line = a.sPt + sb * kPtBytes + krow * 128;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c)
+        *reinterpret_cast<uint4*>(line + ((((2 * c + half) ^ (krow & 7)) & 7) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    }
     if (key >= a.kv_end) {
       // a cache slot past the key range: zero its value columns so P = 0 meets V = 0
-      uint8_t* row = a.sKv + sb * kSlotBytes + krow * 128;
+      uint8_t* row = a.sKv + (t % G::kStages) * G::kSlot + krow * G::kRowBytes;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint4*>(row + (4 * half + c) * kKvChunkBytes + 16 * j) = make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < G::kRowBytes / 16; ++j)
+          *reinterpret_cast<uint4*>(row + (4 * half + c) * G::kChunkBytes + 16 * j) = make_uint4(0, 0, 0, 0);
     }
     ptx::fence_async_smem();
     ptx::tc_fence_before();
@@ -459,10 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int bad = (p.seq_lens[u->b] != r->ctx || p.q_lens[u->b] != r->q) ? 1 : 0;
     if (bad) report(p.status, MLA_DEVICE_PLAN_MISMATCH);
     ms->abort = bad;
-    ptx::mbar_init(&ms->bar_q, 1);
-    for (int i = 0; i < 2; ++i) {
+    ptx::mbar_init(&ms->bar_q, kFp8 ? 4 : 1);  // e4m3: the softmax warps convert Q themselves
+    for (int i = 0; i < 4; ++i) {
       ptx::mbar_init(&ms->kv_full[i], 1);
       ptx::mbar_init(&ms->kv_empty[i], kMmaWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&ms->p_full[i], 4);
       ptx::mbar_init(&ms->pt_empty[i], kMmaWarps);
     }
@@ -491,21 +576,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sKv = smem + kOffKv;
   uint8_t* sPt = smem + kOffPt;
+  using G = Geo<kFp8>;
+  constexpr int S = G::kStages;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     int issued = 0;
     bool q_issued = false;
     if (!*abort) {
-      q_issued = true;
+      q_issued = !kFp8;
       if (lane == 0) {
-        ptx::prefetch_tmap(&tmap_q);
         ptx::prefetch_tmap(&tmap_kv);
-        ptx::mbar_arrive_expect_tx(&ms->bar_q, kQBytes);
-        ptx::tma_load_3d(sQ, &tmap_q, &ms->bar_q, 0, qrow0, 0);
+        if (!kFp8) {
+          ptx::prefetch_tmap(&tmap_q);
+          ptx::mbar_arrive_expect_tx(&ms->bar_q, kQBytes);
+          ptx::tma_load_3d(sQ, &tmap_q, &ms->bar_q, 0, qrow0, 0);
+        }
       }
       const int32_t* pt_row = p.page_table + (size_t)b * p.pt_stride + kv_begin / kPage;
-      for (int t0 = 0; t0 < ntiles && !*abort; t0 += 32) {
+      // page ids 32 at a time (one per lane); the next batch is read ahead so that the L2
+      // prefetch kPrefetchPages beyond the current page can cross a batch boundary
+      auto load_ids = [&](int t0) {
         int pid = 0;
         if (t0 + lane < ntiles) {
           pid = pt_row[t0 + lane];
@@ -514,36 +605,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             pid = 0;
           }
         }
+        return pid;
+      };
+      int pid_cur = load_ids(0);
+      int pid_next = ntiles > 32 ? load_ids(32) : 0;
+      for (int t = 0; t < min(ntiles, kPrefetchPages + S); ++t) {
+        const int pg = __shfl_sync(0xffffffffu, pid_cur, t);
+        if (lane == 0) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, pg * kPage, 0);
+      }
+      __syncwarp();
+      for (int t0 = 0; t0 < ntiles && !*abort; t0 += 32) {
         const int cnt = min(32, ntiles - t0);
         for (int i = 0; i < cnt; ++i) {
-          const int page = __shfl_sync(0xffffffffu, pid, i);
-          const int t = t0 + i, slot = t & 1;
+          const int page = __shfl_sync(0xffffffffu, pid_cur, i);
+          const int tp = i + kPrefetchPages + S;  // page to bring into L2 now (relative to t0)
+          const int page_pf = __shfl_sync(0xffffffffu, tp < 32 ? pid_cur : pid_next, tp & 31);
+          const int t = t0 + i, slot = t % S;
           int ok = 1;
           if (lane == 0) {
-            if (t >= 2) ok = wait_bar(&ms->kv_empty[slot], ((t - 2) >> 1) & 1, abort, p.status);
+            if (t >= S) ok = wait_bar(&ms->kv_empty[slot], ((t - S) / S) & 1, abort, p.status);
             if (ok) {
-              uint8_t* dst = sKv + slot * kSlotBytes;
-              if (kFp8) {
-                ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], kChunks * kFp8ChunkBytes);
-                ptx::tma_load_3d(dst + kFp8StageOff, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0);
-              } else {
-                ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], kSlotBytes);
-                ptx::tma_load_3d(dst, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0);
-              }
+              ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], G::kSlot);
+              ptx::tma_load_3d(sKv + slot * G::kSlot, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0);
+              if (t0 + tp < ntiles) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, page_pf * kPage, 0);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           issued = t + 1;
         }
+        pid_cur = pid_next;
+        pid_next = (t0 + 64 < ntiles) ? load_ids(t0 + 64) : 0;
       }
     }
-    // Drain: every issued copy must land before the CTA may exit (at most the last two
+    // Drain: every issued copy must land before the CTA may exit (at most the last S
     // pages can still be in flight; earlier ones were consumed by the MMAs).
     if (lane == 0) {
-      for (int t = max(0, issued - 2); t < issued; ++t) {
+      for (int t = max(0, issued - S); t < issued; ++t) {
         long long t0c = clock64();
-        while (!ptx::mbar_try_wait(&ms->kv_full[t & 1], (t >> 1) & 1) && clock64() - t0c < kWaitBudget) {
+        while (!ptx::mbar_try_wait(&ms->kv_full[t % S], (t / S) & 1) && clock64() - t0c < kWaitBudget) {
         }
       }
       if (q_issued) {
@@ -553,19 +653,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp <= kMmaWarps) {
-    // ------------------------------------------------------------ MMA issue (+ fp8 expand)
+    // ------------------------------------------------------------ MMA issue
     const int pw = warp - 1;                   // 0..3
-    const int c_lo = chunk_lo(pw), c_hi = chunk_lo(pw + 1);
     const uint32_t sq = ptx::smem_addr(sQ), skv = ptx::smem_addr(sKv), spt = ptx::smem_addr(sPt);
-    const uint32_t idesc_s = ptx::idesc_bf16(64, nmma, 0, 0);    // S^T: K-major K tile, K-major Q
-    const uint32_t idesc_o = ptx::idesc_bf16(128, nmma, 1, 1);   // O^T: MN-major V^T, MN-major P^T
+    // S^T: K-major K tile, K-major Q; O^T: MN-major V^T, MN-major P^T
+    const uint32_t idesc_s = kFp8 ? ptx::idesc_e4m3(64, nmma, 0, 0) : ptx::idesc_bf16(64, nmma, 0, 0);
+    const uint32_t idesc_o = kFp8 ? ptx::idesc_e4m3(128, nmma, 1, 1) : ptx::idesc_bf16(128, nmma, 1, 1);
     const uint32_t d_s = tmem + kTmemS + 64 * pw, d_o = tmem + kTmemO + 64 * pw;
-    uint32_t gphase = 0;
     bool ok = !*abort && warp_wait(&ms->bar_q, 0, abort, p.status);
     bool issued_any = false;
     // Event loop: issue whichever product is ready, O^T first. S^T(t1) needs page t1 and
     // the softmax's read of S^T(t1-1); O^T(t2) needs P^T(t2). O^T(t2) must not wait for
-    // page t2+1, or the slot of page t2 (and so the load of page t2+2) would be held back.
+    // page t2+1, or the slot of page t2 (and so a later page's load) would be held back.
     int t1 = 0, t2 = 0;
     long long idle_t0 = clock64();
     while (ok && t2 < ntiles) {
@@ -574,17 +673,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         int rdy = 0;
         if (lane == 0) rdy = ptx::mbar_test_wait(&ms->p_full[t2 & 1], (t2 >> 1) & 1);
         if (__shfl_sync(0xffffffffu, rdy, 0)) {
-          const int ub = t2 & 1;
+          const int ub = t2 & 1, slot = t2 % S;
           ptx::tc_fence_after();
           if (lane == 0) {
-            const uint32_t v0 = skv + ub * kSlotBytes + 2 * pw * kKvChunkBytes, pt0 = spt + ub * kPtBytes;
+            // value columns [128 pw, 128 pw + 128) = chunks 2 pw, 2 pw + 1 of the page
+            const uint32_t v0 = skv + slot * G::kSlot + 2 * pw * G::kChunkBytes, pt0 = spt + ub * kPtBytes;
+            if constexpr (kFp8) {
+              // K = 32 keys per MMA; P^T = hi + lo parts (64 keys x 64 bytes each)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint64_t ad = ptx::smem_desc(v0 + 2048 * k, kKvChunkBytes, 1024, ptx::kSwizzle128B);
-              uint64_t bd = ptx::smem_desc(pt0 + 2048 * k, 8192, 1024, ptx::kSwizzle128B);
-              ptx::mma_bf16_ss(d_o, ad, bd, idesc_o, (t2 > 0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < 2; ++k)
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                  uint64_t ad = ptx::smem_desc(v0 + 2048 * k, G::kChunkBytes, 512, ptx::kSwizzle64B);
+                  uint64_t bd = ptx::smem_desc(pt0 + part * (kTileKeys * 64) + 2048 * k, 4096, 512, ptx::kSwizzle64B);
+                  ptx::mma_e4m3_ss(d_o, ad, bd, idesc_o, (t2 > 0 || k > 0 || part > 0) ? 1u : 0u);
+                }
+            } else {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                uint64_t ad = ptx::smem_desc(v0 + 2048 * k, G::kChunkBytes, 1024, ptx::kSwizzle128B);
+                uint64_t bd = ptx::smem_desc(pt0 + 2048 * k, 8192, 1024, ptx::kSwizzle128B);
+                ptx::mma_bf16_ss(d_o, ad, bd, idesc_o, (t2 > 0 || k > 0) ? 1u : 0u);
+              }
             }
-            ptx::mma_commit(&ms->kv_empty[ub]);
+            ptx::mma_commit(&ms->kv_empty[slot]);
             ptx::mma_commit(&ms->pt_empty[ub]);
           }
           __syncwarp();
@@ -595,84 +707,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t1 < ntiles && t1 <= t2 + 1) {
         int rdy = 0;
         if (lane == 0)
-          rdy = ptx::mbar_test_wait(&ms->kv_full[t1 & 1], (t1 >> 1) & 1) &&
+          rdy = ptx::mbar_test_wait(&ms->kv_full[t1 % S], (t1 / S) & 1) &&
                 (t1 == 0 || ptx::mbar_test_wait(&ms->s_empty, (t1 - 1) & 1));
         if (__shfl_sync(0xffffffffu, rdy, 0)) {
-          const int slot = t1 & 1;
-          if (kFp8) {
-            // this warp's chunks: read every e4m3 byte first (the bf16 rows overwrite the
-            // e4m3 staging area of other chunks), then write the bf16 rows. Lane l reads the
-            // 16-byte pieces l, l+32, ... of a chunk (conflict-free): key 8i + l/4, columns
-            // 16 (l%4) .. 16 (l%4) + 15.
-            uint8_t* base = sKv + slot * kSlotBytes;
-            uint4 raw[3][8];
-#pragma unroll
-            for (int ci = 0; ci < 3; ++ci)
-              if (c_lo + ci < c_hi)
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  raw[ci][i] = *reinterpret_cast<const uint4*>(base + kFp8StageOff + (c_lo + ci) * kFp8ChunkBytes +
-                                                               i * 512 + 16 * lane);
-            ok = group_sync(&ms->grp_mma, gphase, abort, p.status);
-            if (!ok) break;
-            const int j = lane & 3;
-            // one warp-uniform decision per page: integer expansion unless this warp's share
-            // holds a code that needs the exact conversion (zero, subnormal, NaN)
-            uint32_t special = 0;
-#pragma unroll
-            for (int ci = 0; ci < 3; ++ci)
-              if (c_lo + ci < c_hi)
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  special |= e4m3x4_special(raw[ci][i].x) | e4m3x4_special(raw[ci][i].y) |
-                             e4m3x4_special(raw[ci][i].z) | e4m3x4_special(raw[ci][i].w);
-            if (!__any_sync(0xffffffffu, special != 0u)) {
-#pragma unroll
-              for (int ci = 0; ci < 3; ++ci)
-                if (c_lo + ci < c_hi)
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) {
-                    const int key = 8 * i + (lane >> 2);
-                    uint8_t* line = base + (c_lo + ci) * kKvChunkBytes + key * 128;
-                    uint4 o0, o1;
-                    e4m3x4_to_bf16x4_normal(raw[ci][i].x, o0.x, o0.y);
-                    e4m3x4_to_bf16x4_normal(raw[ci][i].y, o0.z, o0.w);
-                    e4m3x4_to_bf16x4_normal(raw[ci][i].z, o1.x, o1.y);
-                    e4m3x4_to_bf16x4_normal(raw[ci][i].w, o1.z, o1.w);
-                    *reinterpret_cast<uint4*>(line + (((2 * j) ^ (key & 7)) << 4)) = o0;
-                    *reinterpret_cast<uint4*>(line + (((2 * j + 1) ^ (key & 7)) << 4)) = o1;
-                  }
-            } else {
-#pragma unroll
-              for (int ci = 0; ci < 3; ++ci)
-                if (c_lo + ci < c_hi)
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) {
-                    const int key = 8 * i + (lane >> 2);
-                    uint8_t* line = base + (c_lo + ci) * kKvChunkBytes + key * 128;
-                    uint4 o0, o1;
-                    e4m3x4_to_bf16x4_cvt(raw[ci][i].x, o0.x, o0.y);
-                    e4m3x4_to_bf16x4_cvt(raw[ci][i].y, o0.z, o0.w);
-                    e4m3x4_to_bf16x4_cvt(raw[ci][i].z, o1.x, o1.y);
-                    e4m3x4_to_bf16x4_cvt(raw[ci][i].w, o1.z, o1.w);
-                    *reinterpret_cast<uint4*>(line + (((2 * j) ^ (key & 7)) << 4)) = o0;
-                    *reinterpret_cast<uint4*>(line + (((2 * j + 1) ^ (key & 7)) << 4)) = o1;
-                  }
-            }
-            ptx::fence_async_smem();
-            // the K-steps of this warp's S^T MMAs span chunks expanded by other warps
-            ok = group_sync(&ms->grp_mma, gphase, abort, p.status);
-            if (!ok) break;
-          }
           ptx::tc_fence_after();
           if (lane == 0) {
-            const uint32_t a0 = skv + slot * kSlotBytes;
+            const uint32_t a0 = skv + (t1 % S) * G::kSlot;
+            if constexpr (kFp8) {
+              // 18 K-steps of 32 columns x (Q hi, Q lo) = 36 MMAs, 9 per warp
 #pragma unroll
-            for (int i = 0; i < kKStepsPerWarp; ++i) {
-              const int ks = kKStepsPerWarp * pw + i, c = ks >> 2, k = ks & 3;
-              uint64_t ad = ptx::smem_desc(a0 + c * kKvChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
-              uint64_t bd = ptx::smem_desc(sq + c * kQChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
-              ptx::mma_bf16_ss(d_s, ad, bd, idesc_s, i != 0 ? 1u : 0u);
+              for (int i = 0; i < 9; ++i) {
+                const int idx = 9 * pw + i, ks = idx >> 1, part = idx & 1, c = ks >> 1, kk = ks & 1;
+                uint64_t ad = ptx::smem_desc(a0 + c * G::kChunkBytes + 32 * kk, 16, 512, ptx::kSwizzle64B);
+                uint64_t bd = ptx::smem_desc(sq + part * G::kQPartBytes + c * (kRowsCap * 64) + 32 * kk, 16, 512,
+                                             ptx::kSwizzle64B);
+                ptx::mma_e4m3_ss(d_s, ad, bd, idesc_s, i != 0 ? 1u : 0u);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < kKStepsPerWarp; ++i) {
+                const int ks = kKStepsPerWarp * pw + i, c = ks >> 2, k = ks & 3;
+                uint64_t ad = ptx::smem_desc(a0 + c * G::kChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
+                uint64_t bd = ptx::smem_desc(sq + c * kQChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
+                ptx::mma_bf16_ss(d_s, ad, bd, idesc_s, i != 0 ? 1u : 0u);
+              }
             }
             ptx::mma_commit(&ms->s_full);
           }
@@ -712,14 +770,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const SoftmaxArgs a{ms, sKv, sPt, tmem, warp & 3, lane, tid - 32 * (kMmaWarps + 1), nrows, qrow0, kv_begin, kv_end,
+    const SoftmaxArgs a{ms, sQ, sKv, sPt, tmem, warp & 3, lane, tid - 32 * (kMmaWarps + 1), nrows, qrow0, kv_begin, kv_end,
                         ntiles, part_row0, ctx, qlen, tok0, abort};
     if (nch == 1)
-      softmax_role<1>(a, p);
+      softmax_role<1, kFp8>(a, p);
     else if (nch == 2)
-      softmax_role<2>(a, p);
+      softmax_role<2, kFp8>(a, p);
     else
-      softmax_role<3>(a, p);
+      softmax_role<3, kFp8>(a, p);
   }
 
   ptx::tc_fence_before();
@@ -784,16 +842,21 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const uint8_t*
   // 2. weighted sum: warp w takes splits w, w+8, ...; each lane takes 4 consecutive columns
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int col = quarter * 128 + 4 * lane;
+  const float* base = part_o + (size_t)(m.part_row0 + row) * kDv + col;
+  const size_t split_stride = (size_t)m.nrows * kDv;
   int s = warp;
-  for (; s + 8 < ns; s += 16) {
-    const float4 a = *reinterpret_cast<const float4*>(part_o + (size_t)(m.part_row0 + s * m.nrows + row) * kDv + col);
-    const float4 c = *reinterpret_cast<const float4*>(part_o + (size_t)(m.part_row0 + (s + 8) * m.nrows + row) * kDv + col);
-    const float wa = w_s[s], wc = w_s[s + 8];
-    acc.x += wa * a.x + wc * c.x; acc.y += wa * a.y + wc * c.y;
-    acc.z += wa * a.z + wc * c.z; acc.w += wa * a.w + wc * c.w;
+  for (; s + 24 < ns; s += 32) {  // four independent loads in flight per lane
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldcs(reinterpret_cast<const float4*>(base + (size_t)(s + 8 * u) * split_stride));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = w_s[s + 8 * u];
+      acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;
+    }
   }
   for (; s < ns; s += 8) {
-    const float4 a = *reinterpret_cast<const float4*>(part_o + (size_t)(m.part_row0 + s * m.nrows + row) * kDv + col);
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(base + (size_t)s * split_stride));
     const float wa = w_s[s];
     acc.x += wa * a.x; acc.y += wa * a.y; acc.z += wa * a.z; acc.w += wa * a.w;
   }
@@ -880,7 +943,7 @@ static CUresult encode_chunked(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMa
   cuuint32_t es[3] = {1, 1, 1};
   return enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             fp8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
@@ -933,6 +996,8 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
 
   Params prm;
   prm.plan = (const uint8_t*)plan_dev;
+  prm.q = (const __nv_bfloat16*)q;
+  prm.q_rows = h->total_q * h->num_heads;
   prm.page_table = page_table;
   prm.pt_stride = page_table_stride;
   prm.num_pages = num_pages;
@@ -941,7 +1006,7 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
   prm.q_lens = q_lens;
   const float ks = fp8 ? kv_scale : 1.0f;
   prm.score_scale_log2 = sm_scale * ks * 1.4426950408889634f;
-  prm.out_scale = ks;
+  prm.out_scale = fp8 ? ks / kPScaleFp8 : ks;  // the e4m3 path accumulates P times 2^6
   prm.out = (__nv_bfloat16*)out;
   prm.lse = lse;
   prm.part_o = (float*)workspace;

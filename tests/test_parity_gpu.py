@@ -56,8 +56,8 @@ def test_edge_shapes(seq, q, H):
 
 
 def test_fp8_zero_and_subnormal_codes():
-    """Zero (both signs) and subnormal e4m3 codes in visible keys take the exact
-    expansion path; the rest of the page takes the integer path."""
+    """Zero (both signs) and subnormal e4m3 codes in visible keys, and one page of zero
+    codes, go straight into the e4m3 tensor-core products."""
     prob = inputs.make_problem(12, [64 * 5 + 9], [4], FP8, seed=2450)
     g = torch.Generator().manual_seed(3)
     rows = prob.kv.shape[0]
@@ -65,6 +65,22 @@ def test_fp8_zero_and_subnormal_codes():
     codes = torch.tensor([0x00, 0x80, 0x01, 0x87, 0x05, 0x83], dtype=torch.uint8)
     prob.kv.view(-1)[idx] = codes[torch.randint(0, len(codes), (4000,), generator=g)]
     prob.kv[64:128] = 0  # one whole page of zero codes
+    _check(prob)
+
+
+def test_fp8_query_rows_of_very_different_magnitude():
+    """The e4m3 path scales each query row by its own power of two before splitting it
+    into two e4m3 parts: rows from 2^-14 to 2^3 times the usual size, an all-zero row and
+    a row with one large entry must all come out right."""
+    prob = inputs.make_problem(12, [64 * 9 + 17], [4], FP8, seed=2460)
+    q = prob.q.float()
+    rows = q.reshape(-1, 576)
+    for r in range(rows.shape[0]):
+        rows[r] *= 2.0 ** (-14 + (r * 7) % 18)
+    rows[5] = 0
+    rows[11] = 0
+    rows[11, 300] = 6.0
+    prob.q = rows.reshape(prob.q.shape).to(torch.bfloat16)
     _check(prob)
 
 
