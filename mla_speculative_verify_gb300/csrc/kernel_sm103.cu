@@ -17,20 +17,27 @@
 // r52 changes": the latent K stages are held until PV).
 //
 // One thread issues a tcgen05.mma only every ~60 cycles, while an N = 16..48 MMA
-// needs 20..45 cycles of tensor time, so four warps issue in parallel: warp 1+p owns
-// K-chunks of the S^T product (into its own partial accumulator S_p, summed by the
-// softmax) and dv block p of the O^T product.
+// needs 20..45 cycles of tensor time, so S^T is issued by two warps into two partial
+// accumulators (summed by the softmax) and O^T by two more. S^T is double-buffered in
+// tensor memory, so the product of the next page runs while the softmax works on this
+// one.
 //
-// Warp roles (one CTA per SM, one page in flight while the other is consumed):
-//   warp 0     TMA producer: the Q tile once, then one page per stage
-//   warps 1-4  MMA issue (one elected lane each); for an fp8 cache they first expand
-//              their own chunks of the e4m3 page to bf16 in place (exact; kv_scale is
-//              folded into the score and output scales)
+// Warp roles (one CTA per SM):
+//   warp 0     TMA producer: the Q tile once (bf16 cache), then one page per stage
+//              (two bf16 stages, or four e4m3 stages, in the same ring)
+//   warps 1-2  S^T issue (one elected lane each): partial p of S^T(t) into buffer t % 2
+//   warps 3-4  O^T issue: value blocks 2 w, 2 w + 1 of O^T += V^T P^T(t)
 //   warps 5-8  softmax: each thread owns one key of the S^T tile (a TMEM lane); online
 //              softmax with a lazy per-row reference: the reference moves, and O^T is
-//              rescaled in TMEM, only when a score exceeds it by kRefSlack octaves (the
+//              rescaled in TMEM, only when a score exceeds it by a few octaves (the
 //              conditional rescale of flashinfer PR #5602); then the epilogue: O / l to
-//              bf16 out and LSE, or fp32 partials for the merge kernel
+//              bf16 out and LSE, or fp32 partials for the merge kernel. The four warps
+//              agree on every decision through OR-reducing named barriers.
+//
+// For an e4m3 cache the products run on kind::f8f6f4 MMAs straight from the cached
+// codes: each Q row is scaled by a power of two and split into two e4m3 parts (hi and
+// lo), and P into two e4m3 parts as well, so no page is ever expanded to bf16 and the
+// only rounding beyond fp32 accumulation is that of the lo parts (~2^-8 relative).
 //
 // Every mbarrier wait is bounded; on expiry the kernel ORs MLA_DEVICE_WAIT_TIMEOUT into
 // the status word, stops the unit, drains its in-flight copies and frees its TMEM.
@@ -86,7 +93,7 @@ constexpr int kMmaWarps = 4;
 constexpr int kThreads = 32 * (1 + kMmaWarps + 4);  // producer, MMA warps, softmax warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;       // O^T block b at columns 64 b (N <= 64)
-constexpr uint32_t kTmemS = 256;     // partial S^T p at columns 256 + 64 p
+constexpr uint32_t kTmemS = 256;     // S^T buffer b, partial p at columns 256 + 128 b + 64 p
 constexpr float kRefSlack = 8.0f;    // octaves a score may exceed the row reference before it moves
 // e4m3 path: a smaller slack (p <= 4) so that P can be stored times 2^6 (<= 256 < 448,
 // the largest e4m3) and small probabilities stay above e4m3's subnormal range
@@ -94,17 +101,6 @@ constexpr float kRefSlackFp8 = 2.0f;
 constexpr float kPScaleFp8 = 64.0f;
 constexpr int kPrefetchPages = 4;    // pages brought into L2 ahead of the two shared-memory stages
 constexpr long long kWaitBudget = 2000000000LL;  // cycles (~1 s) before a wait gives up
-
-// K-steps (16 columns each) of the S^T product owned by MMA warp p: [9 p, 9 p + 9) of
-// the 36; the e4m3 expansion of a page is split by 64-column chunks instead
-// ([chunk_lo(p), chunk_lo(p + 1)) = 3, 2, 2, 2 of the 9 chunks).
-constexpr int kKSteps = kChunks * 4;
-constexpr int kKStepsPerWarp = kKSteps / 4;
-__host__ __device__ __forceinline__ int chunk_lo(int p) { return p == 0 ? 0 : 1 + 2 * p; }
-
-// Rows of an M = 64 accumulator occupy 16 TMEM lanes per 32-lane quadrant:
-// row r -> lane 32 * (r / 16) + r % 16.
-__device__ __forceinline__ int m64_row_of_lane(int quadrant, int lane) { return lane < 16 ? quadrant * 16 + lane : -1; }
 
 struct Params {
   const uint8_t* plan;
@@ -126,15 +122,13 @@ struct Params {
 struct Misc {
   uint64_t bar_q;
   uint64_t kv_full[4], kv_empty[4];
-  uint64_t s_full, s_empty;
+  uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], pt_empty[2];
-  uint64_t mma_done;
-  uint64_t grp_softmax, grp_mma;  // bounded barriers among the 4 warps of a group
+  uint64_t mma_done[4];
   uint32_t tmem_base;
   int abort;
   int unit[8];
   int req[4];
-  int flags[2][4];
   alignas(16) float ref[64];  // read as float4
   alignas(16) float alpha[64];
   alignas(16) int lim[64];
@@ -171,15 +165,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Barrier among the four warps of a group, built on an mbarrier (count 4) so that it
-// is bounded like every other wait: a warp that gave up never leaves the others stuck.
-__device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, volatile int* abort, int32_t* status) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar);
-  const bool ok = warp_wait(bar, phase & 1, abort, status);
-  ++phase;
-  return ok;
-}
+// Barriers among the four softmax warps only (named barrier 1, 128 threads). Every
+// softmax warp reaches every one of them the same number of times, whatever happens
+// to the unit: decisions that end the loop are taken from a barrier's OR-reduction,
+// so all four warps take them together.
+constexpr uint32_t kSoftmaxBar = 1;
+__device__ __forceinline__ void softmax_sync() { ptx::bar_sync(kSoftmaxBar, 128); }
+__device__ __forceinline__ bool softmax_any(bool pred) { return ptx::bar_red_or(kSoftmaxBar, 128, pred); }
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -230,13 +222,13 @@ template <int NCH, bool kFp8>
 __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params& p) {
   constexpr int NC = 8 * NCH;
   using G = Geo<kFp8>;
+  constexpr float kSlack = kFp8 ? kRefSlackFp8 : kRefSlack;
   Misc* ms = a.ms;
   const int lane = a.lane, qd = a.qd, sidx = a.sidx;
   const int half = lane >> 4;
   const int krow = qd * 16 + (lane & 15);  // key row of this thread in the 64-key tile
   const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
   volatile int* abort = a.abort;
-  uint32_t gphase = 0;
   if (sidx < 64) {
     int lim = 0;
     if (sidx < a.nrows) {
@@ -292,75 +284,74 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&ms->bar_q);
   }
-  bool ok = group_sync(&ms->grp_softmax, gphase, abort, p.status) && !*abort;
+  // `stop` only ever changes through a barrier's reduction, so it is the same in all
+  // four warps; `fail` is this warp's own: one of its bounded waits gave up.
+  bool stop = softmax_any(*abort != 0);
+  bool fail = false;
   int lim_min = a.kv_end;
   for (int n = 0; n < a.nrows; ++n) lim_min = min(lim_min, ms->lim[n]);
   float l_acc[NC];
 #pragma unroll
   for (int i = 0; i < NC; ++i) l_acc[i] = 0.f;
   const float scale = p.score_scale_log2;
-  for (int t = 0; ok && t < a.ntiles; ++t) {
+  for (int t = 0; !stop && t < a.ntiles; ++t) {
     const int sb = t & 1;
-    ok = warp_wait(&ms->s_full, t & 1, abort, p.status);
-    if (!ok) break;
-    ptx::tc_fence_after();
-    // S^T = sum of the four partial accumulators, then split the columns over the halves
     float x[NC];
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      float s0[16], s1[16], s2[16];
-      ptx::tmem_ld16(a.tmem + kTmemS + lane_off + 16 * c, s0);
-      ptx::tmem_ld16(a.tmem + kTmemS + 64 + lane_off + 16 * c, s1);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 16; ++j) s0[j] += s1[j];
-      ptx::tmem_ld16(a.tmem + kTmemS + 128 + lane_off + 16 * c, s1);
-      ptx::tmem_ld16(a.tmem + kTmemS + 192 + lane_off + 16 * c, s2);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 16; ++j) s0[j] += s1[j] + s2[j];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float hi = __shfl_sync(0xffffffffu, s0[8 + j], lane & 15);
-        x[8 * c + j] = half ? hi : s0[j];
-      }
-    }
-    ptx::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&ms->s_empty);
-    const int key = a.kv_begin + t * kTileKeys + krow;
-    const int tile_last = a.kv_begin + t * kTileKeys + kTileKeys - 1;
-    const bool unmasked = tile_last < a.kv_end && tile_last < lim_min;  // tile-uniform fast path
     bool need = false;
+    if (!fail) fail = !warp_wait(&ms->s_full[sb], (t >> 1) & 1, abort, p.status);
+    if (!fail) {
+      ptx::tc_fence_after();
+      // S^T = sum of the two partial accumulators, then split the columns over the halves
+      const uint32_t sbase = a.tmem + kTmemS + 128 * sb + lane_off;
 #pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      const int n0 = 16 * c + 8 * half;
-      const float4 r0 = *reinterpret_cast<const float4*>(&ms->ref[n0]);
-      const float4 r1 = *reinterpret_cast<const float4*>(&ms->ref[n0 + 4]);
-      const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-      float cs[8];
-      if constexpr (kFp8) {
-        const float4 c0 = *reinterpret_cast<const float4*>(&ms->colscale[n0]);
-        const float4 c1 = *reinterpret_cast<const float4*>(&ms->colscale[n0 + 4]);
-        cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w; cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
-      } else {
+      for (int c = 0; c < NCH; ++c) {
+        float s0[16], s1[16];
+        ptx::tmem_ld16(sbase + 16 * c, s0);
+        ptx::tmem_ld16(sbase + 64 + 16 * c, s1);
+        ptx::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cs[j] = scale;
+        for (int j = 0; j < 16; ++j) s0[j] += s1[j];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float hi = __shfl_sync(0xffffffffu, s0[8 + j], lane & 15);
+          x[8 * c + j] = half ? hi : s0[j];
+        }
       }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ms->s_empty[sb]);
+      const int key = a.kv_begin + t * kTileKeys + krow;
+      const int tile_last = a.kv_begin + t * kTileKeys + kTileKeys - 1;
+      const bool unmasked = tile_last < a.kv_end && tile_last < lim_min;  // tile-uniform fast path
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float v = x[8 * c + j] * cs[j];
-        if (!unmasked) v = (key < a.kv_end && key < ms->lim[n0 + j]) ? v : -INFINITY;
-        x[8 * c + j] = v;
-        need |= v > rr[j] + (kFp8 ? kRefSlackFp8 : kRefSlack);
+      for (int c = 0; c < NCH; ++c) {
+        const int n0 = 16 * c + 8 * half;
+        const float4 r0 = *reinterpret_cast<const float4*>(&ms->ref[n0]);
+        const float4 r1 = *reinterpret_cast<const float4*>(&ms->ref[n0 + 4]);
+        const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        float cs[8];
+        if constexpr (kFp8) {
+          const float4 c0 = *reinterpret_cast<const float4*>(&ms->colscale[n0]);
+          const float4 c1 = *reinterpret_cast<const float4*>(&ms->colscale[n0 + 4]);
+          cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w; cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) cs[j] = scale;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float v = x[8 * c + j] * cs[j];
+          if (!unmasked) v = (key < a.kv_end && key < ms->lim[n0 + j]) ? v : -INFINITY;
+          x[8 * c + j] = v;
+          need |= v > rr[j] + kSlack;
+        }
       }
     }
-    const unsigned vote = __any_sync(0xffffffffu, need);
-    if (lane == 0) ms->flags[sb][qd] = vote ? 1 : 0;
-    ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
-    if (!ok) break;
-    const bool moved = ms->flags[sb][0] | ms->flags[sb][1] | ms->flags[sb][2] | ms->flags[sb][3];
-    if (moved) {
+    if (softmax_any(need || fail)) {
+      if (softmax_any(fail || *abort != 0)) {
+        stop = true;
+        break;
+      }
       // column maxima over this tile's keys (16 keys per half-warp), then move each
       // row's reference up to its maximum
 #pragma unroll
@@ -370,8 +361,7 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
         for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if ((lane & 15) == 0) ms->colred[qd][16 * (i / 8) + 8 * half + (i % 8)] = m;
       }
-      ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
-      if (!ok) break;
+      softmax_sync();
       if (sidx < 16 * NCH) {
         const float cm = fmaxf(fmaxf(ms->colred[0][sidx], ms->colred[1][sidx]), fmaxf(ms->colred[2][sidx], ms->colred[3][sidx]));
         const float old = ms->ref[sidx];
@@ -379,31 +369,32 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
         ms->alpha[sidx] = (nw == old) ? 1.f : ex2(old - nw);
         ms->ref[sidx] = nw;
       }
-      ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
-      if (!ok) break;
+      softmax_sync();
 #pragma unroll
       for (int i = 0; i < NC; ++i) l_acc[i] *= ms->alpha[16 * (i / 8) + 8 * half + (i % 8)];
       if (t >= 1) {
         // O^T holds tiles < t: wait for PV(t-1), then scale each row's column by alpha
-        ok = warp_wait(&ms->pt_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, p.status);
-        if (!ok) break;
-        ptx::tc_fence_after();
+        fail = !warp_wait(&ms->pt_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, p.status);
+        if (!fail) {
+          ptx::tc_fence_after();
 #pragma unroll 1
-        for (int blk = 0; blk < 4; ++blk) {
+          for (int blk = 0; blk < 4; ++blk) {
 #pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            float o[16];
-            const uint32_t ta = a.tmem + kTmemO + 64 * blk + lane_off + 16 * c;
-            ptx::tmem_ld16(ta, o);
-            ptx::tmem_ld_wait();
+            for (int c = 0; c < NCH; ++c) {
+              float o[16];
+              const uint32_t ta = a.tmem + kTmemO + 64 * blk + lane_off + 16 * c;
+              ptx::tmem_ld16(ta, o);
+              ptx::tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) o[j] *= ms->alpha[16 * c + j];
-            ptx::tmem_st16(ta, o);
+              for (int j = 0; j < 16; ++j) o[j] *= ms->alpha[16 * c + j];
+              ptx::tmem_st16(ta, o);
+            }
           }
+          ptx::tmem_st_wait();
         }
-        ptx::tmem_st_wait();
       }
     }
+    if (fail) continue;  // the next tile's vote ends the loop in every warp
     // probabilities relative to the (possibly moved) reference, packed to bf16, or for the
     // e4m3 path times 2^6 and split into hi + lo e4m3 parts
     uint32_t pk[NC / 2];
@@ -433,8 +424,8 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
       }
     }
     if (t >= 2) {
-      ok = warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p.status);
-      if (!ok) break;
+      fail = !warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p.status);
+      if (fail) continue;
     }
     if constexpr (kFp8) {
       // e4m3 P^T hi and lo, MN-major with 64-byte rows (64-byte swizzle): key krow's row
@@ -453,6 +444,7 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
         *reinterpret_cast<uint4*>(line + ((((2 * c + half) ^ (krow & 7)) & 7) << 4)) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
     }
+    const int key = a.kv_begin + t * kTileKeys + krow;
     if (key >= a.kv_end) {
       // a cache slot past the key range: zero its value columns so P = 0 meets V = 0
       uint8_t* row = a.sKv + (t % G::kStages) * G::kSlot + krow * G::kRowBytes;
@@ -468,52 +460,50 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
     if (lane == 0) ptx::mbar_arrive(&ms->p_full[sb]);
   }
   // ------------------------------------------------------------ epilogue
-  if (ok) ok = warp_wait(&ms->pt_empty[(a.ntiles - 1) & 1], ((a.ntiles - 1) >> 1) & 1, abort, p.status);
-  if (ok) {
-    ptx::tc_fence_after();
-#pragma unroll
-    for (int i = 0; i < NC; ++i) {
-      float s = l_acc[i];
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if ((lane & 15) == 0) ms->colred[qd][16 * (i / 8) + 8 * half + (i % 8)] = s;
-    }
-    ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
+  if (!stop) {
+    if (!fail) fail = !warp_wait(&ms->pt_empty[(a.ntiles - 1) & 1], ((a.ntiles - 1) >> 1) & 1, abort, p.status);
+    stop = softmax_any(fail || *abort != 0);
   }
-  if (ok) {
-    if (sidx < a.nrows) {
-      const float L = ms->colred[0][sidx] + ms->colred[1][sidx] + ms->colred[2][sidx] + ms->colred[3][sidx];
-      ms->lsum[sidx] = L;
-      const float lse_v = L > 0.f ? (ms->ref[sidx] + lg2(L)) * 0.69314718055994531f : -INFINITY;
-      if (a.part_row0 < 0) {
-        if (p.lse) p.lse[a.qrow0 + sidx] = lse_v;
-      } else {
-        p.part_lse[a.part_row0 + sidx] = lse_v;
-      }
-    }
-    ok = group_sync(&ms->grp_softmax, gphase, abort, p.status);
+  if (stop) return;
+  ptx::tc_fence_after();
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    float s = l_acc[i];
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((lane & 15) == 0) ms->colred[qd][16 * (i / 8) + 8 * half + (i % 8)] = s;
   }
-  if (ok) {
-    const int dv_in_blk = qd * 32 + lane;
+  softmax_sync();
+  if (sidx < a.nrows) {
+    const float L = ms->colred[0][sidx] + ms->colred[1][sidx] + ms->colred[2][sidx] + ms->colred[3][sidx];
+    ms->lsum[sidx] = L;
+    const float lse_v = L > 0.f ? (ms->ref[sidx] + lg2(L)) * 0.69314718055994531f : -INFINITY;
+    if (a.part_row0 < 0) {
+      if (p.lse) p.lse[a.qrow0 + sidx] = lse_v;
+    } else {
+      p.part_lse[a.part_row0 + sidx] = lse_v;
+    }
+  }
+  softmax_sync();
+  const int dv_in_blk = qd * 32 + lane;
 #pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
-      const int dv = blk * 128 + dv_in_blk;
+  for (int blk = 0; blk < 4; ++blk) {
+    const int dv = blk * 128 + dv_in_blk;
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        float o[16];
-        ptx::tmem_ld16(a.tmem + kTmemO + 64 * blk + lane_off + 16 * c, o);
-        ptx::tmem_ld_wait();
+    for (int c = 0; c < NCH; ++c) {
+      float o[16];
+      ptx::tmem_ld16(a.tmem + kTmemO + 64 * blk + lane_off + 16 * c, o);
+      ptx::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int n = 16 * c + j;
-          if (n < a.nrows) {
-            const float L = ms->lsum[n];
-            const float v = L > 0.f ? o[j] * (p.out_scale / L) : 0.f;
-            if (a.part_row0 < 0)
-              p.out[(size_t)(a.qrow0 + n) * kDv + dv] = __float2bfloat16_rn(v);
-            else
-              p.part_o[(size_t)(a.part_row0 + n) * kDv + dv] = v;
-          }
+      for (int j = 0; j < 16; ++j) {
+        const int n = 16 * c + j;
+        if (n < a.nrows) {
+          const float L = ms->lsum[n];
+          const float v = L > 0.f ? o[j] * (p.out_scale / L) : 0.f;
+          if (a.part_row0 < 0)
+            p.out[(size_t)(a.qrow0 + n) * kDv + dv] = __float2bfloat16_rn(v);
+          else
+            p.part_o[(size_t)(a.part_row0 + n) * kDv + dv] = v;
         }
       }
     }
@@ -545,17 +535,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(&ms->bar_q, kFp8 ? 4 : 1);  // e4m3: the softmax warps convert Q themselves
     for (int i = 0; i < 4; ++i) {
       ptx::mbar_init(&ms->kv_full[i], 1);
-      ptx::mbar_init(&ms->kv_empty[i], kMmaWarps);
+      ptx::mbar_init(&ms->kv_empty[i], 2);  // the two O^T warps
     }
     for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&ms->s_full[i], 2);    // the two S^T warps
+      ptx::mbar_init(&ms->s_empty[i], 4);   // the four softmax warps
       ptx::mbar_init(&ms->p_full[i], 4);
-      ptx::mbar_init(&ms->pt_empty[i], kMmaWarps);
+      ptx::mbar_init(&ms->pt_empty[i], 2);  // the two O^T warps
     }
-    ptx::mbar_init(&ms->s_full, kMmaWarps);
-    ptx::mbar_init(&ms->s_empty, 4);
-    ptx::mbar_init(&ms->mma_done, kMmaWarps);
-    ptx::mbar_init(&ms->grp_softmax, 4);
-    ptx::mbar_init(&ms->grp_mma, kMmaWarps);
+    for (int i = 0; i < 4; ++i) ptx::mbar_init(&ms->mma_done[i], 1);
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -654,30 +642,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp <= kMmaWarps) {
     // ------------------------------------------------------------ MMA issue
-    const int pw = warp - 1;                   // 0..3
     const uint32_t sq = ptx::smem_addr(sQ), skv = ptx::smem_addr(sKv), spt = ptx::smem_addr(sPt);
-    // S^T: K-major K tile, K-major Q; O^T: MN-major V^T, MN-major P^T
-    const uint32_t idesc_s = kFp8 ? ptx::idesc_e4m3(64, nmma, 0, 0) : ptx::idesc_bf16(64, nmma, 0, 0);
-    const uint32_t idesc_o = kFp8 ? ptx::idesc_e4m3(128, nmma, 1, 1) : ptx::idesc_bf16(128, nmma, 1, 1);
-    const uint32_t d_s = tmem + kTmemS + 64 * pw, d_o = tmem + kTmemO + 64 * pw;
     bool ok = !*abort && warp_wait(&ms->bar_q, 0, abort, p.status);
-    bool issued_any = false;
-    // Event loop: issue whichever product is ready, O^T first. S^T(t1) needs page t1 and
-    // the softmax's read of S^T(t1-1); O^T(t2) needs P^T(t2). O^T(t2) must not wait for
-    // page t2+1, or the slot of page t2 (and so a later page's load) would be held back.
-    int t1 = 0, t2 = 0;
-    long long idle_t0 = clock64();
-    while (ok && t2 < ntiles) {
-      bool progressed = false;
-      if (t2 < t1) {
-        int rdy = 0;
-        if (lane == 0) rdy = ptx::mbar_test_wait(&ms->p_full[t2 & 1], (t2 >> 1) & 1);
-        if (__shfl_sync(0xffffffffu, rdy, 0)) {
-          const int ub = t2 & 1, slot = t2 % S;
-          ptx::tc_fence_after();
-          if (lane == 0) {
-            // value columns [128 pw, 128 pw + 128) = chunks 2 pw, 2 pw + 1 of the page
-            const uint32_t v0 = skv + slot * G::kSlot + 2 * pw * G::kChunkBytes, pt0 = spt + ub * kPtBytes;
+    bool issued = false;
+    if (warp <= 2) {
+      // S^T(t) = K . Q^T into buffer t % 2 (K-major K tile, K-major Q), partial pw
+      const int pw = warp - 1;
+      const uint32_t idesc_s = kFp8 ? ptx::idesc_e4m3(64, nmma, 0, 0) : ptx::idesc_bf16(64, nmma, 0, 0);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        ok = warp_wait(&ms->kv_full[t % S], (t / S) & 1, abort, p.status);
+        // the softmax must have read S^T(t - 2) out of this buffer
+        if (ok && t >= 2) ok = warp_wait(&ms->s_empty[t & 1], ((t - 2) >> 1) & 1, abort, p.status);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = skv + (t % S) * G::kSlot;
+          const uint32_t d = tmem + kTmemS + 128 * (t & 1) + 64 * pw;
+          if constexpr (kFp8) {
+            // partial pw = Q part pw (hi or lo) over the 18 K-steps of 32 columns
+            const uint32_t b0 = sq + pw * G::kQPartBytes;
+#pragma unroll
+            for (int ks = 0; ks < 18; ++ks) {
+              const int c = ks >> 1, kk = ks & 1;
+              uint64_t ad = ptx::smem_desc(a0 + c * G::kChunkBytes + 32 * kk, 16, 512, ptx::kSwizzle64B);
+              uint64_t bd = ptx::smem_desc(b0 + c * (kRowsCap * 64) + 32 * kk, 16, 512, ptx::kSwizzle64B);
+              ptx::mma_e4m3_ss(d, ad, bd, idesc_s, ks != 0 ? 1u : 0u);
+            }
+          } else {
+            // partial pw = K-steps [18 pw, 18 pw + 18) of the 36 (16 columns each)
+#pragma unroll
+            for (int i = 0; i < 18; ++i) {
+              const int ks = 18 * pw + i, c = ks >> 2, k = ks & 3;
+              uint64_t ad = ptx::smem_desc(a0 + c * G::kChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
+              uint64_t bd = ptx::smem_desc(sq + c * kQChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
+              ptx::mma_bf16_ss(d, ad, bd, idesc_s, i != 0 ? 1u : 0u);
+            }
+          }
+          ptx::mma_commit(&ms->s_full[t & 1]);
+        }
+        __syncwarp();
+        issued = true;
+      }
+    } else {
+      // O^T += V^T . P^T(t) (MN-major V^T, MN-major P^T), value blocks 2 ow and 2 ow + 1
+      const int ow = warp - 3;
+      const uint32_t idesc_o = kFp8 ? ptx::idesc_e4m3(128, nmma, 1, 1) : ptx::idesc_bf16(128, nmma, 1, 1);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        ok = warp_wait(&ms->p_full[t & 1], (t >> 1) & 1, abort, p.status);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const int slot = t % S;
+          const uint32_t pt0 = spt + (t & 1) * kPtBytes;
+#pragma unroll
+          for (int bb = 0; bb < 2; ++bb) {
+            const int blk = 2 * ow + bb;
+            // value columns [128 blk, 128 blk + 128) = chunks 2 blk, 2 blk + 1 of the page
+            const uint32_t v0 = skv + slot * G::kSlot + 2 * blk * G::kChunkBytes;
+            const uint32_t d = tmem + kTmemO + 64 * blk;
             if constexpr (kFp8) {
               // K = 32 keys per MMA; P^T = hi + lo parts (64 keys x 64 bytes each)
 #pragma unroll
@@ -686,84 +708,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int part = 0; part < 2; ++part) {
                   uint64_t ad = ptx::smem_desc(v0 + 2048 * k, G::kChunkBytes, 512, ptx::kSwizzle64B);
                   uint64_t bd = ptx::smem_desc(pt0 + part * (kTileKeys * 64) + 2048 * k, 4096, 512, ptx::kSwizzle64B);
-                  ptx::mma_e4m3_ss(d_o, ad, bd, idesc_o, (t2 > 0 || k > 0 || part > 0) ? 1u : 0u);
+                  ptx::mma_e4m3_ss(d, ad, bd, idesc_o, (t > 0 || k > 0 || part > 0) ? 1u : 0u);
                 }
             } else {
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 uint64_t ad = ptx::smem_desc(v0 + 2048 * k, G::kChunkBytes, 1024, ptx::kSwizzle128B);
                 uint64_t bd = ptx::smem_desc(pt0 + 2048 * k, 8192, 1024, ptx::kSwizzle128B);
-                ptx::mma_bf16_ss(d_o, ad, bd, idesc_o, (t2 > 0 || k > 0) ? 1u : 0u);
+                ptx::mma_bf16_ss(d, ad, bd, idesc_o, (t > 0 || k > 0) ? 1u : 0u);
               }
             }
-            ptx::mma_commit(&ms->kv_empty[slot]);
-            ptx::mma_commit(&ms->pt_empty[ub]);
           }
-          __syncwarp();
-          ++t2;
-          progressed = true;
+          ptx::mma_commit(&ms->kv_empty[slot]);
+          ptx::mma_commit(&ms->pt_empty[t & 1]);
         }
-      }
-      if (t1 < ntiles && t1 <= t2 + 1) {
-        int rdy = 0;
-        if (lane == 0)
-          rdy = ptx::mbar_test_wait(&ms->kv_full[t1 % S], (t1 / S) & 1) &&
-                (t1 == 0 || ptx::mbar_test_wait(&ms->s_empty, (t1 - 1) & 1));
-        if (__shfl_sync(0xffffffffu, rdy, 0)) {
-          ptx::tc_fence_after();
-          if (lane == 0) {
-            const uint32_t a0 = skv + (t1 % S) * G::kSlot;
-            if constexpr (kFp8) {
-              // 18 K-steps of 32 columns x (Q hi, Q lo) = 36 MMAs, 9 per warp
-#pragma unroll
-              for (int i = 0; i < 9; ++i) {
-                const int idx = 9 * pw + i, ks = idx >> 1, part = idx & 1, c = ks >> 1, kk = ks & 1;
-                uint64_t ad = ptx::smem_desc(a0 + c * G::kChunkBytes + 32 * kk, 16, 512, ptx::kSwizzle64B);
-                uint64_t bd = ptx::smem_desc(sq + part * G::kQPartBytes + c * (kRowsCap * 64) + 32 * kk, 16, 512,
-                                             ptx::kSwizzle64B);
-                ptx::mma_e4m3_ss(d_s, ad, bd, idesc_s, i != 0 ? 1u : 0u);
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < kKStepsPerWarp; ++i) {
-                const int ks = kKStepsPerWarp * pw + i, c = ks >> 2, k = ks & 3;
-                uint64_t ad = ptx::smem_desc(a0 + c * G::kChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
-                uint64_t bd = ptx::smem_desc(sq + c * kQChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
-                ptx::mma_bf16_ss(d_s, ad, bd, idesc_s, i != 0 ? 1u : 0u);
-              }
-            }
-            ptx::mma_commit(&ms->s_full);
-          }
-          __syncwarp();
-          issued_any = true;
-          ++t1;
-          progressed = true;
-        }
-      }
-      if (progressed) {
-        idle_t0 = clock64();
-      } else {
-        __nanosleep(32);  // leave issue slots to the softmax warps on this SM sub-partition
-        int stop = 0;
-        if (lane == 0) {
-          if (*abort) {
-            stop = 1;
-          } else if (clock64() - idle_t0 > kWaitBudget) {
-            *abort = 1;
-            report(p.status, MLA_DEVICE_WAIT_TIMEOUT);
-            stop = 1;
-          }
-        }
-        if (__shfl_sync(0xffffffffu, stop, 0)) ok = false;
+        __syncwarp();
+        issued = true;
       }
     }
     // every MMA this warp issued must retire before TMEM is released
-    if (issued_any) {
+    if (issued) {
       if (lane == 0) {
-        ptx::mma_commit(&ms->mma_done);
+        uint64_t* done = &ms->mma_done[warp - 1];
+        ptx::mma_commit(done);
         long long t0c = clock64();
-        while (!ptx::mbar_try_wait(&ms->mma_done, 0) && clock64() - t0c < kWaitBudget) {
-          if (*abort) break;  // the other MMA warps may not commit; the tensor core drains anyway
+        while (!ptx::mbar_try_wait(done, 0) && clock64() - t0c < kWaitBudget) {
         }
       }
       __syncwarp();
