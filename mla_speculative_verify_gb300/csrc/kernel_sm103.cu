@@ -95,15 +95,16 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;       // O^T block b at columns 64 b (N <= 64)
 constexpr uint32_t kTmemS = 256;     // S^T buffer b, partial p at columns 256 + 128 b + 64 p
 constexpr float kRefSlack = 8.0f;    // octaves a score may exceed the row reference before it moves
-// e4m3 path: a smaller slack (p <= 4) so that P can be stored times 2^6 (<= 256 < 448,
-// the largest e4m3) and small probabilities stay above e4m3's subnormal range
-constexpr float kRefSlackFp8 = 2.0f;
-constexpr float kPScaleFp8 = 64.0f;
+// e4m3 path: a smaller slack (p <= 16) so that P can be stored times 2^4 (<= 256 < 448,
+// the largest e4m3); probabilities down to 2^-10 of the reference stay in e4m3's normal
+// range, smaller ones keep an absolute error below 2^-14
+constexpr float kRefSlackFp8 = 4.0f;
+constexpr float kPScaleFp8 = 16.0f;
 constexpr int kPrefetchPages = 4;    // pages brought into L2 ahead of the two shared-memory stages
 constexpr long long kWaitBudget = 2000000000LL;  // cycles (~1 s) before a wait gives up
 
 struct Params {
-  const uint8_t* plan;
+  const PlanUnit* units;   // the plan's unit table (one record per CTA)
   const __nv_bfloat16* q;  // the e4m3 path converts its Q tile from global memory
   int q_rows;              // rows of q (sum q_lens * H)
   const int32_t* page_table;
@@ -127,8 +128,7 @@ struct Misc {
   uint64_t mma_done[4];
   uint32_t tmem_base;
   int abort;
-  int unit[8];
-  int req[4];
+  int unit[12];  // this CTA's PlanUnit
   alignas(16) float ref[64];  // read as float4
   alignas(16) float alpha[64];
   alignas(16) int lim[64];
@@ -210,7 +210,7 @@ struct SoftmaxArgs {
   uint8_t* sKv;
   uint8_t* sPt;
   uint32_t tmem;
-  int qd, lane, sidx, nrows, qrow0, kv_begin, kv_end, ntiles, part_row0, ctx, qlen, tok0;
+  int qd, lane, sidx, b, nrows, qrow0, kv_begin, kv_end, ntiles, part_row0, ctx, qlen, tok0;
   volatile int* abort;
 };
 
@@ -229,6 +229,11 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
   const int krow = qd * 16 + (lane & 15);  // key row of this thread in the 64-key tile
   const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
   volatile int* abort = a.abort;
+  if (sidx == 0 && (p.seq_lens[a.b] != a.ctx || p.q_lens[a.b] != a.qlen)) {
+    // the device lengths differ from those the plan was built for: stop the unit
+    report(p.status, MLA_DEVICE_PLAN_MISMATCH);
+    *a.abort = 1;
+  }
   if (sidx < 64) {
     int lim = 0;
     if (sidx < a.nrows) {
@@ -379,15 +384,18 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
           ptx::tc_fence_after();
 #pragma unroll 1
           for (int blk = 0; blk < 4; ++blk) {
+            float o[NCH][16];
+            const uint32_t ta = a.tmem + kTmemO + 64 * blk + lane_off;
 #pragma unroll
             for (int c = 0; c < NCH; ++c) {
-              float o[16];
-              const uint32_t ta = a.tmem + kTmemO + 64 * blk + lane_off + 16 * c;
-              ptx::tmem_ld16(ta, o);
+              ptx::tmem_ld16(ta + 16 * c, o[c]);
               ptx::tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < 16; ++j) o[j] *= ms->alpha[16 * c + j];
-              ptx::tmem_st16(ta, o);
+              for (int j = 0; j < 16; j += 4) {
+                const float4 al = *reinterpret_cast<const float4*>(&ms->alpha[16 * c + j]);
+                o[c][j] *= al.x; o[c][j + 1] *= al.y; o[c][j + 2] *= al.z; o[c][j + 3] *= al.w;
+              }
+              ptx::tmem_st16(ta + 16 * c, o[c]);
             }
           }
           ptx::tmem_st_wait();
@@ -396,7 +404,7 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
     }
     if (fail) continue;  // the next tile's vote ends the loop in every warp
     // probabilities relative to the (possibly moved) reference, packed to bf16, or for the
-    // e4m3 path times 2^6 and split into hi + lo e4m3 parts
+    // e4m3 path times 2^4 and split into hi + lo e4m3 parts
     uint32_t pk[NC / 2];
     uint32_t ph[NC / 4], pl[NC / 4];
 #pragma unroll
@@ -522,17 +530,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   ptx::pdl_launch_dependents();
 
-  const PlanHeader* ph = (const PlanHeader*)p.plan;
-  if (tid == 0) {
-    const PlanUnit* u = (const PlanUnit*)(p.plan + ph->units_off) + blockIdx.x;
-    const PlanRequest* r = (const PlanRequest*)(p.plan + ph->req_off) + u->b;
-    ms->unit[0] = u->b; ms->unit[1] = u->qrow0; ms->unit[2] = u->nrows; ms->unit[3] = u->kv_begin;
-    ms->unit[4] = u->kv_end; ms->unit[5] = u->part_row0;
-    ms->req[0] = r->ctx; ms->req[1] = r->q; ms->req[2] = r->tok0;
-    int bad = (p.seq_lens[u->b] != r->ctx || p.q_lens[u->b] != r->q) ? 1 : 0;
-    if (bad) report(p.status, MLA_DEVICE_PLAN_MISMATCH);
-    ms->abort = bad;
-    ptx::mbar_init(&ms->bar_q, kFp8 ? 4 : 1);  // e4m3: the softmax warps convert Q themselves
+  // Prologue. Warp 0 reads this CTA's unit record (one round trip), issues the Q copy and
+  // reads the first page ids before the CTA-wide barrier, so that the first page copies
+  // leave as early as possible. The device copies of seq_lens / q_lens are checked
+  // against the plan by the softmax warps afterwards.
+  constexpr int kUnitWords = (int)(sizeof(PlanUnit) / 4);
+  using G = Geo<kFp8>;
+  constexpr int S = G::kStages;
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sKv = smem + kOffKv;
+  uint8_t* sPt = smem + kOffPt;
+  int pid_cur = 0, pid_next = 0;  // producer: page ids of 32 consecutive pages, and of the next 32
+  if (warp == 0) {
+    if (lane == 0) {
+      ms->abort = 0;
+      ptx::mbar_init(&ms->bar_q, kFp8 ? 4 : 1);  // e4m3: the softmax warps convert Q themselves
     for (int i = 0; i < 4; ++i) {
       ptx::mbar_init(&ms->kv_full[i], 1);
       ptx::mbar_init(&ms->kv_empty[i], 2);  // the two O^T warps
@@ -545,8 +557,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 4; ++i) ptx::mbar_init(&ms->mma_done[i], 1);
     ptx::fence_mbar_init();
-  }
-  if (warp == 1) {
+    }
+    int uw = 0;
+    if (lane < kUnitWords) uw = reinterpret_cast<const int32_t*>(p.units + blockIdx.x)[lane];
+    if (lane < kUnitWords) ms->unit[lane] = uw;
+    const int ub = __shfl_sync(0xffffffffu, uw, 0), uq0 = __shfl_sync(0xffffffffu, uw, 1);
+    const int ukb = __shfl_sync(0xffffffffu, uw, 3), uke = __shfl_sync(0xffffffffu, uw, 4);
+    const int unt = (uke - ukb + kTileKeys - 1) / kTileKeys;
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmap_kv);
+      if (!kFp8) {
+        ptx::prefetch_tmap(&tmap_q);
+        ptx::mbar_arrive_expect_tx(&ms->bar_q, kQBytes);
+        ptx::tma_load_3d(sQ, &tmap_q, &ms->bar_q, 0, uq0, 0);
+      }
+    }
+    const int32_t* pt_row = p.page_table + (size_t)ub * p.pt_stride + ukb / kPage;
+    pid_cur = lane < unt ? pt_row[lane] : 0;
+    pid_next = 32 + lane < unt ? pt_row[32 + lane] : 0;
+  } else if (warp == 1) {
     ptx::tmem_alloc(&ms->tmem_base, kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -556,47 +585,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int b = ms->unit[0], qrow0 = ms->unit[1], nrows = ms->unit[2];
   const int kv_begin = ms->unit[3], kv_end = ms->unit[4], part_row0 = ms->unit[5];
-  const int ctx = ms->req[0], qlen = ms->req[1], tok0 = ms->req[2];
+  const int ctx = ms->unit[8], qlen = ms->unit[9], tok0 = ms->unit[10];
   const int ntiles = (kv_end - kv_begin + kTileKeys - 1) / kTileKeys;
   const int nmma = (nrows + 15) & ~15;   // MMA N (rows rounded up to 16)
   const int nch = nmma / 16;             // 16-column chunks of S^T / O^T
   const uint32_t tmem = ms->tmem_base;
-  uint8_t* sQ = smem + kOffQ;
-  uint8_t* sKv = smem + kOffKv;
-  uint8_t* sPt = smem + kOffPt;
-  using G = Geo<kFp8>;
-  constexpr int S = G::kStages;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     int issued = 0;
-    bool q_issued = false;
-    if (!*abort) {
-      q_issued = !kFp8;
-      if (lane == 0) {
-        ptx::prefetch_tmap(&tmap_kv);
-        if (!kFp8) {
-          ptx::prefetch_tmap(&tmap_q);
-          ptx::mbar_arrive_expect_tx(&ms->bar_q, kQBytes);
-          ptx::tma_load_3d(sQ, &tmap_q, &ms->bar_q, 0, qrow0, 0);
-        }
-      }
+    const bool q_issued = !kFp8;
+    {
       const int32_t* pt_row = p.page_table + (size_t)b * p.pt_stride + kv_begin / kPage;
       // page ids 32 at a time (one per lane); the next batch is read ahead so that the L2
-      // prefetch kPrefetchPages beyond the current page can cross a batch boundary
-      auto load_ids = [&](int t0) {
-        int pid = 0;
-        if (t0 + lane < ntiles) {
-          pid = pt_row[t0 + lane];
-          if (pid < 0 || pid >= p.num_pages) {
-            report(p.status, MLA_DEVICE_BAD_PAGE);
-            pid = 0;
-          }
+      // prefetch kPrefetchPages beyond the current page can cross a batch boundary. An id
+      // outside the cache is reported and replaced by page 0.
+      auto checked = [&](int pid, int t) {
+        if (t < ntiles && (pid < 0 || pid >= p.num_pages)) {
+          report(p.status, MLA_DEVICE_BAD_PAGE);
+          pid = 0;
         }
         return pid;
       };
-      int pid_cur = load_ids(0);
-      int pid_next = ntiles > 32 ? load_ids(32) : 0;
+      auto load_ids = [&](int t0) { return checked(t0 + lane < ntiles ? pt_row[t0 + lane] : 0, t0 + lane); };
+      pid_cur = checked(pid_cur, lane);
+      pid_next = checked(pid_next, 32 + lane);
       for (int t = 0; t < min(ntiles, kPrefetchPages + S); ++t) {
         const int pg = __shfl_sync(0xffffffffu, pid_cur, t);
         if (lane == 0) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, pg * kPage, 0);
@@ -739,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const SoftmaxArgs a{ms, sQ, sKv, sPt, tmem, warp & 3, lane, tid - 32 * (kMmaWarps + 1), nrows, qrow0, kv_begin, kv_end,
+    const SoftmaxArgs a{ms, sQ, sKv, sPt, tmem, warp & 3, lane, tid - 32 * (kMmaWarps + 1), b, nrows, qrow0, kv_begin, kv_end,
                         ntiles, part_row0, ctx, qlen, tok0, abort};
     if (nch == 1)
       softmax_role<1, kFp8>(a, p);
@@ -758,30 +771,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ LSE merge
-// One CTA per (packed row, quarter of the 512 value columns): 8 warps share the
+// One CTA per (packed row, quarter of the 512 value columns): 16 warps share the
 // splits of the row. L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s; a split that
-// a causal row cannot see has L_s = -inf and weight 0.
-constexpr int kMergeThreads = 256;
+// a causal row cannot see has L_s = -inf and weight 0. The first batch of partial-O
+// loads is issued before the LSE reduction, so that both wait on memory together.
+constexpr int kMergeThreads = 512;
+constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergeBatch = 8;  // partial-O loads in flight per lane
 constexpr int kMergeMaxSplits = 2048;
 
-__global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const uint8_t* plan, const float* part_o,
+__global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const PlanMerge* merges, const float* part_o,
                                                                  const float* part_lse, __nv_bfloat16* out, float* lse) {
   ptx::pdl_wait_primary();
   __shared__ float w_s[kMergeMaxSplits];
-  __shared__ float red[8][2];
-  __shared__ float4 acc_s[8][32];
-  const PlanHeader* ph = (const PlanHeader*)plan;
-  const PlanMerge m = ((const PlanMerge*)(plan + ph->merge_off))[blockIdx.y];
+  __shared__ float red[kMergeWarps][2];
+  __shared__ float4 acc_s[kMergeWarps][32];
+  const PlanMerge m = merges[blockIdx.y];
   const int row = blockIdx.x >> 2, quarter = blockIdx.x & 3;
   if (row >= m.nrows) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ns = m.n_splits;  // the planner keeps this <= kMergeMaxSplits
+  const int col = quarter * 128 + 4 * lane;
+  const float* base = part_o + (size_t)(m.part_row0 + row) * kDv + col;
+  const size_t split_stride = (size_t)m.nrows * kDv;
+  float4 v[kMergeBatch];
+#pragma unroll
+  for (int u = 0; u < kMergeBatch; ++u) {
+    const int s = warp + kMergeWarps * u;
+    v[u] = s < ns ? __ldcs(reinterpret_cast<const float4*>(base + (size_t)s * split_stride)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   // 1. L over the splits
   float mx = -INFINITY;
   for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
-    const float v = part_lse[m.part_row0 + s * m.nrows + row];
-    w_s[s] = v;
-    mx = fmaxf(mx, v);
+    const float x = part_lse[m.part_row0 + s * m.nrows + row];
+    w_s[s] = x;
+    mx = fmaxf(mx, x);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -789,11 +813,11 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const uint8_t*
   __syncthreads();
   mx = red[0][0];
 #pragma unroll
-  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i][0]);
+  for (int i = 1; i < kMergeWarps; ++i) mx = fmaxf(mx, red[i][0]);
   float sum = 0.f;
   for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
-    const float v = w_s[s];
-    sum += v == -INFINITY ? 0.f : __expf(v - mx);
+    const float x = w_s[s];
+    sum += x == -INFINITY ? 0.f : __expf(x - mx);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -801,42 +825,41 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const uint8_t*
   __syncthreads();
   sum = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) sum += red[i][1];
+  for (int i = 0; i < kMergeWarps; ++i) sum += red[i][1];
   const float L = mx + __logf(sum);
   for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
-    const float v = w_s[s];
-    w_s[s] = v == -INFINITY ? 0.f : __expf(v - L);
+    const float x = w_s[s];
+    w_s[s] = x == -INFINITY ? 0.f : __expf(x - L);
   }
   __syncthreads();
-  // 2. weighted sum: warp w takes splits w, w+8, ...; each lane takes 4 consecutive columns
+  // 2. weighted sum: warp w takes splits w, w + 16, ...; each lane 4 consecutive columns
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int col = quarter * 128 + 4 * lane;
-  const float* base = part_o + (size_t)(m.part_row0 + row) * kDv + col;
-  const size_t split_stride = (size_t)m.nrows * kDv;
-  int s = warp;
-  for (; s + 24 < ns; s += 32) {  // four independent loads in flight per lane
-    float4 v[4];
+  for (int s0 = 0;;) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = __ldcs(reinterpret_cast<const float4*>(base + (size_t)(s + 8 * u) * split_stride));
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float w = w_s[s + 8 * u];
-      acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const int s = s0 + warp + kMergeWarps * u;
+      if (s < ns) {
+        const float w = w_s[s];
+        acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;
+      }
     }
-  }
-  for (; s < ns; s += 8) {
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(base + (size_t)s * split_stride));
-    const float wa = w_s[s];
-    acc.x += wa * a.x; acc.y += wa * a.y; acc.z += wa * a.z; acc.w += wa * a.w;
+    s0 += kMergeWarps * kMergeBatch;
+    if (s0 >= ns) break;
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const int s = s0 + warp + kMergeWarps * u;
+      v[u] = s < ns ? __ldcs(reinterpret_cast<const float4*>(base + (size_t)s * split_stride))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   acc_s[warp][lane] = acc;
   __syncthreads();
   if (warp == 0) {
     float4 r = acc_s[0][lane];
 #pragma unroll
-    for (int i = 1; i < 8; ++i) {
-      const float4 v = acc_s[i][lane];
-      r.x += v.x; r.y += v.y; r.z += v.z; r.w += v.w;
+    for (int i = 1; i < kMergeWarps; ++i) {
+      const float4 x = acc_s[i][lane];
+      r.x += x.x; r.y += x.y; r.z += x.z; r.w += x.w;
     }
     const int qr = m.qrow0 + row;
     uint2 pk = make_uint2(pack_bf16(r.x, r.y), pack_bf16(r.z, r.w));
@@ -964,7 +987,7 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
   if (r != CUDA_SUCCESS) return set_error(MLA_ERR_CUDA, "tensor map for kv_cache failed (CUresult %d)", (int)r);
 
   Params prm;
-  prm.plan = (const uint8_t*)plan_dev;
+  prm.units = (const PlanUnit*)((const uint8_t*)plan_dev + h->units_off);
   prm.q = (const __nv_bfloat16*)q;
   prm.q_rows = h->total_q * h->num_heads;
   prm.page_table = page_table;
@@ -975,7 +998,7 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
   prm.q_lens = q_lens;
   const float ks = fp8 ? kv_scale : 1.0f;
   prm.score_scale_log2 = sm_scale * ks * 1.4426950408889634f;
-  prm.out_scale = fp8 ? ks / kPScaleFp8 : ks;  // the e4m3 path accumulates P times 2^6
+  prm.out_scale = fp8 ? ks / kPScaleFp8 : ks;  // the e4m3 path accumulates P times 2^4
   prm.out = (__nv_bfloat16*)out;
   prm.lse = lse;
   prm.part_o = (float*)workspace;
@@ -1000,7 +1023,8 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    ce = cudaLaunchKernelEx(&cfg, lse_merge_kernel, (const uint8_t*)plan_dev, (const float*)prm.part_o,
+    ce = cudaLaunchKernelEx(&cfg, lse_merge_kernel, (const PlanMerge*)((const uint8_t*)plan_dev + h->merge_off),
+                            (const float*)prm.part_o,
                             (const float*)prm.part_lse, (__nv_bfloat16*)out, lse);
     if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "merge kernel launch: %s", cudaGetErrorString(ce));
   }

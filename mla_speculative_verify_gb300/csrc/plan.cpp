@@ -144,6 +144,7 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
         u.kv_begin = kb; u.kv_end = ke;
         u.part_row0 = n_split > 1 ? part0[t - i] + s * tiles[t].nrows : -1;
         u.split = s; u.n_splits = n_split;
+        u.ctx = reqs[b].ctx; u.q = reqs[b].q; u.tok0 = reqs[b].tok0; u.reserved = 0;
         units.push_back(u);
       }
     }

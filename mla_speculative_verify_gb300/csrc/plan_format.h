@@ -8,7 +8,7 @@
 namespace mla {
 
 constexpr uint32_t kPlanMagic = 0x564C4D41u;  // "AMLV"
-constexpr uint32_t kPlanVersion = 2;
+constexpr uint32_t kPlanVersion = 3;
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kPage = 64;
@@ -42,7 +42,10 @@ struct PlanUnit {
   int32_t part_row0;   // first workspace partial row, or -1: write out/lse directly
   int32_t split;       // split index within the row tile
   int32_t n_splits;    // splits of this row tile
+  int32_t ctx, q, tok0;  // the request's fields, repeated so that a CTA reads one record
+  int32_t reserved;
 };
+static_assert(sizeof(PlanUnit) == 48, "plan unit is 48 bytes");
 
 // One merge item: nrows rows whose n_splits partials sit at part_row0 + s * nrows.
 struct PlanMerge {

@@ -51,6 +51,9 @@ def test_plan_invariants(seq_lens, q_lens, H, num_sms):
         assert u["kv_begin"] % 64 == 0
         assert u["kv_end"] % 64 == 0 or u["kv_end"] == ctx
         assert 1 <= u["nrows"] <= 48
+        # the request fields repeated in the unit record match the request table
+        req = p["requests"][b]
+        assert (u["ctx"], u["q"], u["tok0"]) == (req["ctx"], req["q"], req["tok0"]) == (ctx, q_lens[b], cu[b])
         r0, r1 = u["qrow0"], u["qrow0"] + u["nrows"]
         assert cu[b] * H <= r0 and r1 <= cu[b + 1] * H, "a unit's rows stay inside its request"
         for r in range(r0, r1, max(1, (r1 - r0) // 3)):
