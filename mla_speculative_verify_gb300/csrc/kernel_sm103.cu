@@ -17,15 +17,18 @@
 // r52 changes": the latent K stages are held until PV).
 //
 // One thread issues a tcgen05.mma only every ~60 cycles, while an N = 16..48 MMA
-// needs 20..45 cycles of tensor time, so S^T is issued by two warps into two partial
-// accumulators (summed by the softmax) and O^T by two more. S^T is double-buffered in
+// needs 20..45 cycles of tensor time, so for a bf16 cache S^T is issued by two warps into
+// two partial accumulators (summed by the softmax) and O^T by two more. For an e4m3 cache
+// S^T takes half the MMAs (K = 32) and multiplies each K step by Q_hi and Q_lo at once
+// (N = 2 nmma), so the two S^T warps take alternate pages. S^T is double-buffered in
 // tensor memory, so the product of the next page runs while the softmax works on this
 // one.
 //
 // Warp roles (one CTA per SM):
 //   warp 0     TMA producer: the Q tile once (bf16 cache), then one page per stage
 //              (two bf16 stages, or four e4m3 stages, in the same ring)
-//   warps 1-2  S^T issue (one elected lane each): partial p of S^T(t) into buffer t % 2
+//   warps 1-2  S^T issue (one lane each) into buffer t % 2: bf16 partial p of every
+//              page, or every other page for e4m3
 //   warps 3-4  O^T issue: value blocks 2 w, 2 w + 1 of O^T += V^T P^T(t)
 //   warps 5-8  softmax: each thread owns one key of the S^T tile (a TMEM lane); online
 //              softmax with a lazy per-row reference: the reference moves, and O^T is
@@ -64,6 +67,10 @@ constexpr int kTileKeys = 64;                      // keys per stage = one page
 constexpr int kChunks = 9;                         // 576 = 9 x 64 columns (128-byte swizzle rows)
 constexpr int kQChunkBytes = kRowsCap * 128;       // 6144
 constexpr int kQBytes = kChunks * kQChunkBytes;    // 55296
+// e4m3 path: per 64-column chunk, the Q_hi rows and then the Q_lo rows (<= 2 x 48 rows of
+// 64 bytes, 64-byte swizzle), so that one MMA with N = 2 nmma multiplies K by both parts
+constexpr int kQ8ChunkBytes = 2 * kRowsCap * 64;   // 6144
+static_assert(kChunks * kQ8ChunkBytes <= kQBytes, "e4m3 Q fits the Q region");
 constexpr int kKvChunkBytes = kTileKeys * 128;     // 8192 (bf16 page chunk: 64 keys x 64 columns)
 constexpr int kSlotBytes = kChunks * kKvChunkBytes;  // 73728 (bf16 page)
 constexpr int kKvBytes = 2 * kSlotBytes;           // page ring: two bf16 stages or four e4m3 stages
@@ -85,7 +92,6 @@ struct Geo {
   static constexpr int kRowBytes = kFp8 ? 64 : 128;           // bytes of one key in one chunk
   static constexpr int kChunkBytes = kTileKeys * kRowBytes;   // 4096 / 8192
   static constexpr int kSlot = kChunks * kChunkBytes;         // 36864 / 73728
-  static constexpr int kQPartBytes = kChunks * kRowsCap * 64; // e4m3 Q hi or lo part: 27648
   static_assert(kStages * kSlot == kKvBytes, "ring size");
 };
 
@@ -244,13 +250,13 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
     ms->ref[sidx] = -INFINITY;
   }
   if constexpr (kFp8) {
-    // Q tile -> e4m3 hi + lo parts (64-byte swizzle, K-major) for the e4m3 S^T MMAs. Row r
+    // Q tile -> e4m3 hi rows [0, nmma) and lo rows [nmma, 2 nmma) (64-byte swizzle,
+    // K-major) for the e4m3 S^T MMAs, whose N = 2 nmma columns hold K Q_hi^T and then
+    // K Q_lo^T. Row r
     // is scaled by 2^e_r so that its largest |q| lands in [128, 256); hi = q 2^e_r rounded to
     // e4m3, lo = the remainder in e4m3: hi + lo reproduces the bf16 row to ~2^-17 of its
     // largest entry. 2^-e_r goes into the row's score scale.
     const float base = p.score_scale_log2;
-    uint8_t* q_hi = a.sQ;
-    uint8_t* q_lo = a.sQ + G::kQPartBytes;
     for (int r = qd; r < 16 * NCH; r += 4) {
       const int grow = a.qrow0 + r;
       float v[18];
@@ -279,9 +285,9 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
         const float w0 = v[j] * sc, w1 = v[j + 1] * sc;
         const float h0 = round_to_e4m3_precision(w0), h1 = round_to_e4m3_precision(w1);
         const int col = 18 * lane + j;  // even: the pair stays in one 16-byte piece
-        const int off = (col >> 6) * (kRowsCap * 64) + sw64_offset(r, col & 63);
-        *reinterpret_cast<uint16_t*>(q_hi + off) = (uint16_t)e4m3x2(h0, h1);
-        *reinterpret_cast<uint16_t*>(q_lo + off) = (uint16_t)e4m3x2(w0 - h0, w1 - h1);
+        uint8_t* chunk = a.sQ + (col >> 6) * kQ8ChunkBytes;
+        *reinterpret_cast<uint16_t*>(chunk + sw64_offset(r, col & 63)) = (uint16_t)e4m3x2(h0, h1);
+        *reinterpret_cast<uint16_t*>(chunk + sw64_offset(16 * NCH + r, col & 63)) = (uint16_t)e4m3x2(w0 - h0, w1 - h1);
       }
       if (lane == 0) ms->colscale[r] = base * __uint_as_float((uint32_t)(127 - e) << 23);
     }
@@ -306,13 +312,15 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
     if (!fail) fail = !warp_wait(&ms->s_full[sb], (t >> 1) & 1, abort, p.status);
     if (!fail) {
       ptx::tc_fence_after();
-      // S^T = sum of the two partial accumulators, then split the columns over the halves
+      // S^T = the sum of two accumulator column blocks (bf16: the two partials; e4m3: the
+      // Q_hi and Q_lo products), then split the columns over the halves
       const uint32_t sbase = a.tmem + kTmemS + 128 * sb + lane_off;
+      constexpr uint32_t kSecond = kFp8 ? 16 * NCH : 64;
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         float s0[16], s1[16];
         ptx::tmem_ld16(sbase + 16 * c, s0);
-        ptx::tmem_ld16(sbase + 64 + 16 * c, s1);
+        ptx::tmem_ld16(sbase + kSecond + 16 * c, s1);
         ptx::tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) s0[j] += s1[j];
@@ -550,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&ms->kv_empty[i], 2);  // the two O^T warps
     }
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&ms->s_full[i], 2);    // the two S^T warps
+      ptx::mbar_init(&ms->s_full[i], kFp8 ? 1 : 2);  // the S^T warp(s) of a tile
       ptx::mbar_init(&ms->s_empty[i], 4);   // the four softmax warps
       ptx::mbar_init(&ms->p_full[i], 4);
       ptx::mbar_init(&ms->pt_empty[i], 2);  // the two O^T warps
@@ -659,10 +667,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = !*abort && warp_wait(&ms->bar_q, 0, abort, p.status);
     bool issued = false;
     if (warp <= 2) {
-      // S^T(t) = K . Q^T into buffer t % 2 (K-major K tile, K-major Q), partial pw
+      // S^T(t) = K . Q^T into buffer t % 2 (K-major K tile, K-major Q). bf16: warp 1 + pw
+      // accumulates partial pw of every tile. e4m3: warp 1 + pw issues the tiles with
+      // t % 2 == pw, all 18 K-steps, N = 2 nmma (Q_hi and Q_lo side by side).
       const int pw = warp - 1;
-      const uint32_t idesc_s = kFp8 ? ptx::idesc_e4m3(64, nmma, 0, 0) : ptx::idesc_bf16(64, nmma, 0, 0);
+      const uint32_t idesc_s = kFp8 ? ptx::idesc_e4m3(64, 2 * nmma, 0, 0) : ptx::idesc_bf16(64, nmma, 0, 0);
       for (int t = 0; ok && t < ntiles; ++t) {
+        if (kFp8 && (t & 1) != pw) continue;
         ok = warp_wait(&ms->kv_full[t % S], (t / S) & 1, abort, p.status);
         // the softmax must have read S^T(t - 2) out of this buffer
         if (ok && t >= 2) ok = warp_wait(&ms->s_empty[t & 1], ((t - 2) >> 1) & 1, abort, p.status);
@@ -670,18 +681,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         if (lane == 0) {
           const uint32_t a0 = skv + (t % S) * G::kSlot;
-          const uint32_t d = tmem + kTmemS + 128 * (t & 1) + 64 * pw;
           if constexpr (kFp8) {
-            // partial pw = Q part pw (hi or lo) over the 18 K-steps of 32 columns
-            const uint32_t b0 = sq + pw * G::kQPartBytes;
+            const uint32_t d = tmem + kTmemS + 128 * (t & 1);
 #pragma unroll
             for (int ks = 0; ks < 18; ++ks) {
               const int c = ks >> 1, kk = ks & 1;
               uint64_t ad = ptx::smem_desc(a0 + c * G::kChunkBytes + 32 * kk, 16, 512, ptx::kSwizzle64B);
-              uint64_t bd = ptx::smem_desc(b0 + c * (kRowsCap * 64) + 32 * kk, 16, 512, ptx::kSwizzle64B);
+              uint64_t bd = ptx::smem_desc(sq + c * kQ8ChunkBytes + 32 * kk, 16, 512, ptx::kSwizzle64B);
               ptx::mma_e4m3_ss(d, ad, bd, idesc_s, ks != 0 ? 1u : 0u);
             }
           } else {
+            const uint32_t d = tmem + kTmemS + 128 * (t & 1) + 64 * pw;
             // partial pw = K-steps [18 pw, 18 pw + 18) of the 36 (16 columns each)
 #pragma unroll
             for (int i = 0; i < 18; ++i) {
