@@ -18,7 +18,7 @@
 //
 // One thread issues a tcgen05.mma only every ~60 cycles, while an N = 16..48 MMA
 // needs 20..45 cycles of tensor time, so for a bf16 cache S^T is issued by two warps into
-// two partial accumulators (summed by the softmax) and O^T by two more. For an e4m3 cache
+// two partial accumulators (summed by the softmax) and O^T by a third. For an e4m3 cache
 // S^T takes half the MMAs (K = 32) and multiplies each K step by Q_hi and Q_lo at once
 // (N = 2 nmma), so the two S^T warps take alternate pages. S^T is double-buffered in
 // tensor memory, so the product of the next page runs while the softmax works on this
@@ -29,12 +29,13 @@
 //              (two bf16 stages, or four e4m3 stages, in the same ring)
 //   warps 1-2  S^T issue (one lane each) into buffer t % 2: bf16 partial p of every
 //              page, or every other page for e4m3
-//   warps 3-4  O^T issue: value blocks 2 w, 2 w + 1 of O^T += V^T P^T(t)
-//   warps 5-8  softmax: each thread owns one key of the S^T tile (a TMEM lane); online
+//   warp 3     O^T issue: the four value blocks of O^T += V^T P^T(t)
+//   warps 4-11 softmax: each thread owns one key of the S^T tile (a TMEM lane) and a
+//              quarter of the columns of each 16-column chunk; online
 //              softmax with a lazy per-row reference: the reference moves, and O^T is
 //              rescaled in TMEM, only when a score exceeds it by a few octaves (the
 //              conditional rescale of flashinfer PR #5602); then the epilogue: O / l to
-//              bf16 out and LSE, or fp32 partials for the merge kernel. The four warps
+//              bf16 out and LSE, or fp32 partials for the merge kernel. The eight warps
 //              agree on every decision through OR-reducing named barriers.
 //
 // For an e4m3 cache the products run on kind::f8f6f4 MMAs straight from the cached
@@ -95,8 +96,10 @@ struct Geo {
   static_assert(kStages * kSlot == kKvBytes, "ring size");
 };
 
-constexpr int kMmaWarps = 4;
-constexpr int kThreads = 32 * (1 + kMmaWarps + 4);  // producer, MMA warps, softmax warps
+constexpr int kMmaWarps = 3;      // two S^T issuers, one O^T issuer
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, each owning half of the columns
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kThreads = 32 * (1 + kMmaWarps + kSoftmaxWarps);  // producer, MMA warps, softmax warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;       // O^T block b at columns 64 b (N <= 64)
 constexpr uint32_t kTmemS = 256;     // S^T buffer b, partial p at columns 256 + 128 b + 64 p
@@ -138,7 +141,7 @@ struct Misc {
   alignas(16) float ref[64];  // read as float4
   alignas(16) float alpha[64];
   alignas(16) int lim[64];
-  alignas(16) float colred[4][64];
+  alignas(16) float colred[4][64];  // per TMEM lane quadrant, per packed row
   alignas(16) float lsum[64];
   alignas(16) float colscale[64];  // e4m3 path: score scale of each row (its Q split scale folded in)
 };
@@ -171,13 +174,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Barriers among the four softmax warps only (named barrier 1, 128 threads). Every
-// softmax warp reaches every one of them the same number of times, whatever happens
-// to the unit: decisions that end the loop are taken from a barrier's OR-reduction,
-// so all four warps take them together.
+// Barriers among the softmax warps only (named barrier 1). Every softmax warp reaches
+// every one of them the same number of times, whatever happens to the unit: decisions
+// that end the loop are taken from a barrier's OR-reduction, so all warps take them
+// together.
 constexpr uint32_t kSoftmaxBar = 1;
-__device__ __forceinline__ void softmax_sync() { ptx::bar_sync(kSoftmaxBar, 128); }
-__device__ __forceinline__ bool softmax_any(bool pred) { return ptx::bar_red_or(kSoftmaxBar, 128, pred); }
+__device__ __forceinline__ void softmax_sync() { ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads); }
+__device__ __forceinline__ bool softmax_any(bool pred) { return ptx::bar_red_or(kSoftmaxBar, kSoftmaxThreads, pred); }
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -216,23 +219,25 @@ struct SoftmaxArgs {
   uint8_t* sKv;
   uint8_t* sPt;
   uint32_t tmem;
-  int qd, lane, sidx, b, nrows, qrow0, kv_begin, kv_end, ntiles, part_row0, ctx, qlen, tok0;
+  int qd, grp, lane, sidx, b, nrows, qrow0, kv_begin, kv_end, ntiles, part_row0, ctx, qlen, tok0;
   volatile int* abort;
 };
 
-// Softmax warps for a tile of 16 NCH packed rows. Lanes 0..15 of a warp read their key's
-// S^T row from TMEM (the M = 64 accumulator uses 16 lanes per quadrant) and hand the
-// upper 8 of every 16 columns to lanes 16..31, so each thread works on 8 NCH columns of
-// one key: columns 16 c + 8 half + j, c < NCH, j < 8.
+// Softmax warps for a tile of 16 NCH packed rows. Warp (qd, grp) owns the 16 key rows of
+// TMEM lane quadrant qd (the M = 64 accumulator uses 16 lanes per quadrant) and, of every
+// 16 columns, the 8 columns 8 grp .. 8 grp + 7: lanes 0..15 read them from TMEM and hand
+// the upper 4 to lanes 16..31, so each thread works on 4 NCH columns of one key: columns
+// 16 c + 8 grp + 4 half + j, c < NCH, j < 4.
 template <int NCH, bool kFp8>
 __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params& p) {
-  constexpr int NC = 8 * NCH;
+  constexpr int NC = 4 * NCH;
   using G = Geo<kFp8>;
   constexpr float kSlack = kFp8 ? kRefSlackFp8 : kRefSlack;
   Misc* ms = a.ms;
-  const int lane = a.lane, qd = a.qd, sidx = a.sidx;
+  const int lane = a.lane, qd = a.qd, grp = a.grp, sidx = a.sidx;
   const int half = lane >> 4;
   const int krow = qd * 16 + (lane & 15);  // key row of this thread in the 64-key tile
+  const int col0 = 8 * grp + 4 * half;     // first of this thread's 4 columns in each chunk
   const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
   volatile int* abort = a.abort;
   if (sidx == 0 && (p.seq_lens[a.b] != a.ctx || p.q_lens[a.b] != a.qlen)) {
@@ -252,12 +257,11 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
   if constexpr (kFp8) {
     // Q tile -> e4m3 hi rows [0, nmma) and lo rows [nmma, 2 nmma) (64-byte swizzle,
     // K-major) for the e4m3 S^T MMAs, whose N = 2 nmma columns hold K Q_hi^T and then
-    // K Q_lo^T. Row r
-    // is scaled by 2^e_r so that its largest |q| lands in [128, 256); hi = q 2^e_r rounded to
-    // e4m3, lo = the remainder in e4m3: hi + lo reproduces the bf16 row to ~2^-17 of its
-    // largest entry. 2^-e_r goes into the row's score scale.
+    // K Q_lo^T. Row r is scaled by 2^e_r so that its largest |q| lands in [128, 256);
+    // hi = q 2^e_r rounded to e4m3, lo = the remainder in e4m3: hi + lo reproduces the
+    // bf16 row to ~2^-17 of its largest entry. 2^-e_r goes into the row's score scale.
     const float base = p.score_scale_log2;
-    for (int r = qd; r < 16 * NCH; r += 4) {
+    for (int r = (sidx >> 5); r < 16 * NCH; r += kSoftmaxWarps) {
       const int grow = a.qrow0 + r;
       float v[18];
       if (grow < p.q_rows) {
@@ -296,7 +300,7 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
     if (lane == 0) ptx::mbar_arrive(&ms->bar_q);
   }
   // `stop` only ever changes through a barrier's reduction, so it is the same in all
-  // four warps; `fail` is this warp's own: one of its bounded waits gave up.
+  // softmax warps; `fail` is this warp's own: one of its bounded waits gave up.
   bool stop = softmax_any(*abort != 0);
   bool fail = false;
   int lim_min = a.kv_end;
@@ -313,21 +317,21 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
     if (!fail) {
       ptx::tc_fence_after();
       // S^T = the sum of two accumulator column blocks (bf16: the two partials; e4m3: the
-      // Q_hi and Q_lo products), then split the columns over the halves
-      const uint32_t sbase = a.tmem + kTmemS + 128 * sb + lane_off;
+      // Q_hi and Q_lo products); lanes 0..15 read 8 columns, lanes 16..31 take 4 of them
+      const uint32_t sbase = a.tmem + kTmemS + 128 * sb + lane_off + 8 * grp;
       constexpr uint32_t kSecond = kFp8 ? 16 * NCH : 64;
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
-        float s0[16], s1[16];
-        ptx::tmem_ld16(sbase + 16 * c, s0);
-        ptx::tmem_ld16(sbase + kSecond + 16 * c, s1);
+        float s0[8], s1[8];
+        ptx::tmem_ld8(sbase + 16 * c, s0);
+        ptx::tmem_ld8(sbase + kSecond + 16 * c, s1);
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) s0[j] += s1[j];
+        for (int j = 0; j < 8; ++j) s0[j] += s1[j];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float hi = __shfl_sync(0xffffffffu, s0[8 + j], lane & 15);
-          x[8 * c + j] = half ? hi : s0[j];
+        for (int j = 0; j < 4; ++j) {
+          const float hi = __shfl_sync(0xffffffffu, s0[4 + j], lane & 15);
+          x[4 * c + j] = half ? hi : s0[j];
         }
       }
       ptx::tc_fence_before();
@@ -338,25 +342,18 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
       const bool unmasked = tile_last < a.kv_end && tile_last < lim_min;  // tile-uniform fast path
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
-        const int n0 = 16 * c + 8 * half;
-        const float4 r0 = *reinterpret_cast<const float4*>(&ms->ref[n0]);
-        const float4 r1 = *reinterpret_cast<const float4*>(&ms->ref[n0 + 4]);
-        const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-        float cs[8];
-        if constexpr (kFp8) {
-          const float4 c0 = *reinterpret_cast<const float4*>(&ms->colscale[n0]);
-          const float4 c1 = *reinterpret_cast<const float4*>(&ms->colscale[n0 + 4]);
-          cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w; cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
-        } else {
+        const int n0 = 16 * c + col0;
+        const float4 rr = *reinterpret_cast<const float4*>(&ms->ref[n0]);
+        float4 cs = make_float4(scale, scale, scale, scale);
+        if constexpr (kFp8) cs = *reinterpret_cast<const float4*>(&ms->colscale[n0]);
+        const float rrv[4] = {rr.x, rr.y, rr.z, rr.w};
+        const float csv[4] = {cs.x, cs.y, cs.z, cs.w};
 #pragma unroll
-          for (int j = 0; j < 8; ++j) cs[j] = scale;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float v = x[8 * c + j] * cs[j];
+        for (int j = 0; j < 4; ++j) {
+          float v = x[4 * c + j] * csv[j];
           if (!unmasked) v = (key < a.kv_end && key < ms->lim[n0 + j]) ? v : -INFINITY;
-          x[8 * c + j] = v;
-          need |= v > rr[j] + kSlack;
+          x[4 * c + j] = v;
+          need |= v > rrv[j] + kSlack;
         }
       }
     }
@@ -372,7 +369,7 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
         float m = x[i];
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if ((lane & 15) == 0) ms->colred[qd][16 * (i / 8) + 8 * half + (i % 8)] = m;
+        if ((lane & 15) == 0) ms->colred[qd][16 * (i / 4) + col0 + (i % 4)] = m;
       }
       softmax_sync();
       if (sidx < 16 * NCH) {
@@ -384,26 +381,27 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
       }
       softmax_sync();
 #pragma unroll
-      for (int i = 0; i < NC; ++i) l_acc[i] *= ms->alpha[16 * (i / 8) + 8 * half + (i % 8)];
+      for (int i = 0; i < NC; ++i) l_acc[i] *= ms->alpha[16 * (i / 4) + col0 + (i % 4)];
       if (t >= 1) {
         // O^T holds tiles < t: wait for PV(t-1), then scale each row's column by alpha
+        // (this warp: value blocks 2 grp and 2 grp + 1 of its lane quadrant)
         fail = !warp_wait(&ms->pt_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, p.status);
         if (!fail) {
           ptx::tc_fence_after();
 #pragma unroll 1
-          for (int blk = 0; blk < 4; ++blk) {
-            float o[NCH][16];
+          for (int blk = 2 * grp; blk < 2 * grp + 2; ++blk) {
             const uint32_t ta = a.tmem + kTmemO + 64 * blk + lane_off;
 #pragma unroll
             for (int c = 0; c < NCH; ++c) {
-              ptx::tmem_ld16(ta + 16 * c, o[c]);
+              float o[16];
+              ptx::tmem_ld16(ta + 16 * c, o);
               ptx::tmem_ld_wait();
 #pragma unroll
               for (int j = 0; j < 16; j += 4) {
                 const float4 al = *reinterpret_cast<const float4*>(&ms->alpha[16 * c + j]);
-                o[c][j] *= al.x; o[c][j + 1] *= al.y; o[c][j + 2] *= al.z; o[c][j + 3] *= al.w;
+                o[j] *= al.x; o[j + 1] *= al.y; o[j + 2] *= al.z; o[j + 3] *= al.w;
               }
-              ptx::tmem_st16(ta + 16 * c, o[c]);
+              ptx::tmem_st16(ta + 16 * c, o);
             }
           }
           ptx::tmem_st_wait();
@@ -414,29 +412,28 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
     // probabilities relative to the (possibly moved) reference, packed to bf16, or for the
     // e4m3 path times 2^4 and split into hi + lo e4m3 parts
     uint32_t pk[NC / 2];
-    uint32_t ph[NC / 4], pl[NC / 4];
+    uint32_t ph[NCH], pl[NCH];
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
-      const int n0 = 16 * c + 8 * half;
-      const float4 r0 = *reinterpret_cast<const float4*>(&ms->ref[n0]);
-      const float4 r1 = *reinterpret_cast<const float4*>(&ms->ref[n0 + 4]);
-      const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+      const int n0 = 16 * c + col0;
+      const float4 rr = *reinterpret_cast<const float4*>(&ms->ref[n0]);
+      const float rrv[4] = {rr.x, rr.y, rr.z, rr.w};
+      float pv[4];
 #pragma unroll
-      for (int j = 0; j < 8; j += 2) {
-        const float v0 = x[8 * c + j], v1 = x[8 * c + j + 1];
-        const float p0 = v0 == -INFINITY ? 0.f : ex2(v0 - rr[j]);
-        const float p1 = v1 == -INFINITY ? 0.f : ex2(v1 - rr[j + 1]);
-        l_acc[8 * c + j] += p0;
-        l_acc[8 * c + j + 1] += p1;
-        if constexpr (kFp8) {
-          const float w0 = p0 * kPScaleFp8, w1 = p1 * kPScaleFp8;
-          const float h0 = round_to_e4m3_precision(w0), h1 = round_to_e4m3_precision(w1);
-          const uint32_t hc = e4m3x2(h0, h1), lc = e4m3x2(w0 - h0, w1 - h1);
-          const int k4 = (8 * c + j) / 4, sh = ((8 * c + j) % 4) * 8;
-          if (sh == 0) { ph[k4] = hc; pl[k4] = lc; } else { ph[k4] |= hc << 16; pl[k4] |= lc << 16; }
-        } else {
-          pk[(8 * c + j) / 2] = pack_bf16(p0, p1);
-        }
+      for (int j = 0; j < 4; ++j) {
+        const float v = x[4 * c + j];
+        pv[j] = v == -INFINITY ? 0.f : ex2(v - rrv[j]);
+        l_acc[4 * c + j] += pv[j];
+      }
+      if constexpr (kFp8) {
+        const float w0 = pv[0] * kPScaleFp8, w1 = pv[1] * kPScaleFp8, w2 = pv[2] * kPScaleFp8, w3 = pv[3] * kPScaleFp8;
+        const float h0 = round_to_e4m3_precision(w0), h1 = round_to_e4m3_precision(w1);
+        const float h2 = round_to_e4m3_precision(w2), h3 = round_to_e4m3_precision(w3);
+        ph[c] = e4m3x2(h0, h1) | (e4m3x2(h2, h3) << 16);
+        pl[c] = e4m3x2(w0 - h0, w1 - h1) | (e4m3x2(w2 - h2, w3 - h3) << 16);
+      } else {
+        pk[2 * c] = pack_bf16(pv[0], pv[1]);
+        pk[2 * c + 1] = pack_bf16(pv[2], pv[3]);
       }
     }
     if (t >= 2) {
@@ -449,26 +446,28 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
       uint8_t* line_lo = line_hi + kTileKeys * 64;
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
-        const int off = (((c ^ (krow >> 1)) & 3) << 4) + 8 * half;
-        *reinterpret_cast<uint2*>(line_hi + off) = make_uint2(ph[2 * c], ph[2 * c + 1]);
-        *reinterpret_cast<uint2*>(line_lo + off) = make_uint2(pl[2 * c], pl[2 * c + 1]);
+        const int off = (((c ^ (krow >> 1)) & 3) << 4) + col0;
+        *reinterpret_cast<uint32_t*>(line_hi + off) = ph[c];
+        *reinterpret_cast<uint32_t*>(line_lo + off) = pl[c];
       }
     } else {
       uint8_t* line = a.sPt + sb * kPtBytes + krow * 128;
 #pragma unroll
       for (int c = 0; c < NCH; ++c)
-        *reinterpret_cast<uint4*>(line + ((((2 * c + half) ^ (krow & 7)) & 7) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        *reinterpret_cast<uint2*>(line + ((((2 * c + grp) ^ (krow & 7)) & 7) << 4) + 8 * half) =
+            make_uint2(pk[2 * c], pk[2 * c + 1]);
     }
     const int key = a.kv_begin + t * kTileKeys + krow;
     if (key >= a.kv_end) {
-      // a cache slot past the key range: zero its value columns so P = 0 meets V = 0
+      // a cache slot past the key range: zero its value columns so P = 0 meets V = 0 (this
+      // thread: chunks 2 q4 and 2 q4 + 1, q4 = 2 grp + half)
       uint8_t* row = a.sKv + (t % G::kStages) * G::kSlot + krow * G::kRowBytes;
+      const int q4 = 2 * grp + half;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int j = 0; j < G::kRowBytes / 16; ++j)
-          *reinterpret_cast<uint4*>(row + (4 * half + c) * G::kChunkBytes + 16 * j) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(row + (2 * q4 + c) * G::kChunkBytes + 16 * j) = make_uint4(0, 0, 0, 0);
     }
     ptx::fence_async_smem();
     ptx::tc_fence_before();
@@ -487,7 +486,7 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
     float s = l_acc[i];
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if ((lane & 15) == 0) ms->colred[qd][16 * (i / 8) + 8 * half + (i % 8)] = s;
+    if ((lane & 15) == 0) ms->colred[qd][16 * (i / 4) + col0 + (i % 4)] = s;
   }
   softmax_sync();
   if (sidx < a.nrows) {
@@ -503,7 +502,7 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
   softmax_sync();
   const int dv_in_blk = qd * 32 + lane;
 #pragma unroll 1
-  for (int blk = 0; blk < 4; ++blk) {
+  for (int blk = 2 * grp; blk < 2 * grp + 2; ++blk) {
     const int dv = blk * 128 + dv_in_blk;
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
@@ -552,16 +551,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       ms->abort = 0;
-      ptx::mbar_init(&ms->bar_q, kFp8 ? 4 : 1);  // e4m3: the softmax warps convert Q themselves
+      ptx::mbar_init(&ms->bar_q, kFp8 ? kSoftmaxWarps : 1);  // e4m3: the softmax warps convert Q themselves
     for (int i = 0; i < 4; ++i) {
       ptx::mbar_init(&ms->kv_full[i], 1);
-      ptx::mbar_init(&ms->kv_empty[i], 2);  // the two O^T warps
+      ptx::mbar_init(&ms->kv_empty[i], 1);  // the O^T warp
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&ms->s_full[i], kFp8 ? 1 : 2);  // the S^T warp(s) of a tile
-      ptx::mbar_init(&ms->s_empty[i], 4);   // the four softmax warps
-      ptx::mbar_init(&ms->p_full[i], 4);
-      ptx::mbar_init(&ms->pt_empty[i], 2);  // the two O^T warps
+      ptx::mbar_init(&ms->s_empty[i], kSoftmaxWarps);
+      ptx::mbar_init(&ms->p_full[i], kSoftmaxWarps);
+      ptx::mbar_init(&ms->pt_empty[i], 1);  // the O^T warp
     }
     for (int i = 0; i < 4; ++i) ptx::mbar_init(&ms->mma_done[i], 1);
     ptx::fence_mbar_init();
@@ -707,8 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = true;
       }
     } else {
-      // O^T += V^T . P^T(t) (MN-major V^T, MN-major P^T), value blocks 2 ow and 2 ow + 1
-      const int ow = warp - 3;
+      // O^T += V^T . P^T(t) (MN-major V^T, MN-major P^T), all four value blocks
       const uint32_t idesc_o = kFp8 ? ptx::idesc_e4m3(128, nmma, 1, 1) : ptx::idesc_bf16(128, nmma, 1, 1);
       for (int t = 0; ok && t < ntiles; ++t) {
         ok = warp_wait(&ms->p_full[t & 1], (t >> 1) & 1, abort, p.status);
@@ -718,8 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = t % S;
           const uint32_t pt0 = spt + (t & 1) * kPtBytes;
 #pragma unroll
-          for (int bb = 0; bb < 2; ++bb) {
-            const int blk = 2 * ow + bb;
+          for (int blk = 0; blk < 4; ++blk) {
             // value columns [128 blk, 128 blk + 128) = chunks 2 blk, 2 blk + 1 of the page
             const uint32_t v0 = skv + slot * G::kSlot + 2 * blk * G::kChunkBytes;
             const uint32_t d = tmem + kTmemO + 64 * blk;
@@ -762,7 +759,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const SoftmaxArgs a{ms, sQ, sKv, sPt, tmem, warp & 3, lane, tid - 32 * (kMmaWarps + 1), b, nrows, qrow0, kv_begin, kv_end,
+    const SoftmaxArgs a{ms, sQ, sKv, sPt, tmem, warp & 3, (warp - 1 - kMmaWarps) >> 2, lane,
+                        tid - 32 * (kMmaWarps + 1), b, nrows, qrow0, kv_begin, kv_end,
                         ntiles, part_row0, ctx, qlen, tok0, abort};
     if (nch == 1)
       softmax_role<1, kFp8>(a, p);
