@@ -109,7 +109,6 @@ constexpr float kRefSlack = 8.0f;    // octaves a score may exceed the row refer
 // range, smaller ones keep an absolute error below 2^-14
 constexpr float kRefSlackFp8 = 4.0f;
 constexpr float kPScaleFp8 = 16.0f;
-constexpr int kPrefetchPages = 4;    // pages brought into L2 ahead of the two shared-memory stages
 constexpr long long kWaitBudget = 2000000000LL;  // cycles (~1 s) before a wait gives up
 
 struct Params {
@@ -604,9 +603,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool q_issued = !kFp8;
     {
       const int32_t* pt_row = p.page_table + (size_t)b * p.pt_stride + kv_begin / kPage;
-      // page ids 32 at a time (one per lane); the next batch is read ahead so that the L2
-      // prefetch kPrefetchPages beyond the current page can cross a batch boundary. An id
-      // outside the cache is reported and replaced by page 0.
+      // page ids 32 at a time (one per lane), the next batch read one batch ahead. An id
+      // outside the cache is reported and replaced by page 0. (Prefetching pages into L2
+      // ahead of the ring measured slower: the extra requests queue in front of the loads.)
       auto checked = [&](int pid, int t) {
         if (t < ntiles && (pid < 0 || pid >= p.num_pages)) {
           report(p.status, MLA_DEVICE_BAD_PAGE);
@@ -617,17 +616,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_ids = [&](int t0) { return checked(t0 + lane < ntiles ? pt_row[t0 + lane] : 0, t0 + lane); };
       pid_cur = checked(pid_cur, lane);
       pid_next = checked(pid_next, 32 + lane);
-      for (int t = 0; t < min(ntiles, kPrefetchPages + S); ++t) {
-        const int pg = __shfl_sync(0xffffffffu, pid_cur, t);
-        if (lane == 0) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, pg * kPage, 0);
-      }
-      __syncwarp();
       for (int t0 = 0; t0 < ntiles && !*abort; t0 += 32) {
         const int cnt = min(32, ntiles - t0);
         for (int i = 0; i < cnt; ++i) {
           const int page = __shfl_sync(0xffffffffu, pid_cur, i);
-          const int tp = i + kPrefetchPages + S;  // page to bring into L2 now (relative to t0)
-          const int page_pf = __shfl_sync(0xffffffffu, tp < 32 ? pid_cur : pid_next, tp & 31);
           const int t = t0 + i, slot = t % S;
           int ok = 1;
           if (lane == 0) {
@@ -635,7 +627,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
               ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], G::kSlot);
               ptx::tma_load_3d(sKv + slot * G::kSlot, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0);
-              if (t0 + tp < ntiles) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, page_pf * kPage, 0);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
