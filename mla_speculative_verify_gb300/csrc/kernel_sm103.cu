@@ -867,6 +867,54 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const PlanMerg
   }
 }
 
+// The same merge for plans whose row tiles have at most kMergeSmallSplits splits (ragged
+// batches cut into many short units): one warp per (packed row, quarter of the value
+// columns), all of its partial-O loads issued at once, the LSE reduction done across the
+// warp's lanes (lane s holds split s). A CTA of 8 warps covers two rows.
+constexpr int kMergeSmallSplits = 16;
+constexpr int kMergeSmallWarps = 8;
+
+__global__ void __launch_bounds__(32 * kMergeSmallWarps) lse_merge_small_kernel(const PlanMerge* merges,
+                                                                                const float* part_o,
+                                                                                const float* part_lse,
+                                                                                __nv_bfloat16* out, float* lse) {
+  ptx::pdl_wait_primary();
+  const PlanMerge m = merges[blockIdx.y];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int idx = blockIdx.x * kMergeSmallWarps + warp;
+  const int row = idx >> 2, quarter = idx & 3;
+  if (row >= m.nrows) return;
+  const int ns = m.n_splits;  // <= kMergeSmallSplits (checked on the host)
+  const int col = quarter * 128 + 4 * lane;
+  const float* base = part_o + (size_t)(m.part_row0 + row) * kDv + col;
+  const size_t split_stride = (size_t)m.nrows * kDv;
+  float4 v[kMergeSmallSplits];
+#pragma unroll
+  for (int s = 0; s < kMergeSmallSplits; ++s)
+    v[s] = s < ns ? __ldcs(reinterpret_cast<const float4*>(base + (size_t)s * split_stride))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float x = lane < ns ? part_lse[m.part_row0 + lane * m.nrows + row] : -INFINITY;
+  float mx = x;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float sum = x == -INFINITY ? 0.f : __expf(x - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float L = mx + __logf(sum);
+  const float w = x == -INFINITY ? 0.f : __expf(x - L);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int s = 0; s < kMergeSmallSplits; ++s) {
+    const float ws = __shfl_sync(0xffffffffu, w, s);
+    if (s < ns) {
+      acc.x += ws * v[s].x; acc.y += ws * v[s].y; acc.z += ws * v[s].z; acc.w += ws * v[s].w;
+    }
+  }
+  const int qr = m.qrow0 + row;
+  *reinterpret_cast<uint2*>(out + (size_t)qr * kDv + col) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+  if (lse && quarter == 0 && lane == 0) lse[qr] = L;
+}
+
 int rows_cap_for(int kv_dtype) {
   (void)kv_dtype;
   return kRowsCap;
@@ -1012,9 +1060,15 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
   ce = cudaGetLastError();
   if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "fold kernel launch: %s", cudaGetErrorString(ce));
   if (h->n_merge > 0) {
+    // the warp-per-row merge when every row tile has few splits, else the CTA-per-row one
+    const PlanMerge* mh = (const PlanMerge*)((const uint8_t*)plan_host + h->merge_off);
+    int max_ns = 0;
+    for (int i = 0; i < h->n_merge; ++i) max_ns = max(max_ns, mh[i].n_splits);
+    const bool small = max_ns <= kMergeSmallSplits;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(h->rows_cap * 4), (unsigned)h->n_merge, 1);
-    cfg.blockDim = dim3(kMergeThreads, 1, 1);
+    cfg.gridDim = small ? dim3((unsigned)((h->rows_cap * 4 + kMergeSmallWarps - 1) / kMergeSmallWarps), (unsigned)h->n_merge, 1)
+                        : dim3((unsigned)(h->rows_cap * 4), (unsigned)h->n_merge, 1);
+    cfg.blockDim = dim3(small ? 32 * kMergeSmallWarps : kMergeThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1022,8 +1076,8 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    ce = cudaLaunchKernelEx(&cfg, lse_merge_kernel, (const PlanMerge*)((const uint8_t*)plan_dev + h->merge_off),
-                            (const float*)prm.part_o,
+    ce = cudaLaunchKernelEx(&cfg, small ? lse_merge_small_kernel : lse_merge_kernel,
+                            (const PlanMerge*)((const uint8_t*)plan_dev + h->merge_off), (const float*)prm.part_o,
                             (const float*)prm.part_lse, (__nv_bfloat16*)out, lse);
     if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "merge kernel launch: %s", cudaGetErrorString(ce));
   }

@@ -10,10 +10,12 @@
 //      (the shared-memory budget of one CTA, see kernel_sm103.cu). The tiles of
 //      one group are adjacent in the unit list, so they stream the same pages at
 //      the same time and the second read is served by L2.
-//   3. Each row tile's key range [0, ctx) is cut into page-aligned splits so that
-//      the units fill the SMs; split units write partial (O, LSE) rows that the
+//   3. Each group's key range [0, ctx) is cut into page-aligned splits of about the
+//      per-SM share of the work; split units write partial (O, LSE) rows that the
 //      merge kernel combines.
 #include <algorithm>
+#include <functional>
+#include <queue>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -88,7 +90,6 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
   struct RowTile { int b, qrow0, nrows, pages; };
   std::vector<RowTile> tiles;
   std::vector<PlanRequest> reqs(batch);
-  long long total_page_work = 0;
   int tok0 = 0;
   for (int b = 0; b < batch; ++b) {
     int ctx = seq_lens_h[b], q = q_lens_h[b];
@@ -103,53 +104,119 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
       int grow0 = (tok0 + g * F) * num_heads;
       for (int r0 = 0; r0 < R; r0 += T) {
         tiles.push_back(RowTile{b, grow0 + r0, std::min(T, R - r0), pages});
-        total_page_work += pages;
       }
     }
     tok0 += q;
   }
 
-  // --- splits ----------------------------------------------------------------------
-  int min_pages = o.min_pages_per_split > 0 ? o.min_pages_per_split : 4;
-  long long target_units = num_sms;
-  long long per_unit = std::max<long long>(min_pages, (total_page_work + target_units - 1) / target_units);
-  std::vector<PlanUnit> units;
-  std::vector<PlanMerge> merges;
-  int part_rows = 0;
-  // group the row tiles of one fold group so that equal splits are adjacent
-  size_t i = 0;
-  while (i < tiles.size()) {
-    size_t j = i;  // tiles [i, j) share (b, group): consecutive with equal b and pages, qrow0 contiguous
+  // --- fold groups ------------------------------------------------------------------
+  // tiles [t0, t1) of one fold group: consecutive, same request, qrow0 contiguous
+  struct Group { size_t t0, t1; int b, pages, n_split, cap; };  // cap: piece length in pages (0: equal pieces)
+  std::vector<Group> groups;
+  for (size_t i = 0; i < tiles.size();) {
+    size_t j = i;
     int grp_rows = 0;
     const int b = tiles[i].b;
     const int R = reqs[b].fold * num_heads;
     while (j < tiles.size() && tiles[j].b == b && grp_rows < R) { grp_rows += tiles[j].nrows; ++j; }
-    int pages = tiles[i].pages;
-    int n_split = o.force_splits > 0 ? o.force_splits : (int)((pages + per_unit - 1) / per_unit);
-    n_split = std::max(1, std::min(std::min(n_split, pages), max_splits_for_merge()));
-    std::vector<int> part0(j - i, -1);
+    groups.push_back(Group{i, j, b, tiles[i].pages, 1, 1});
+    i = j;
+  }
+
+  // --- splits ----------------------------------------------------------------------
+  // Each group is cut into pieces of T pages (the last one shorter); all row tiles of the
+  // group are cut at the same boundaries. The units are ordered longest first (below), so
+  // the full-length units fill the SMs and the short tails run back to back on the SMs
+  // left over. T is the per-SM share of the tile-pages divided by k, for the k in 1..4
+  // whose schedule ends first in a model of the hardware's in-order CTA dispatch (each
+  // CTA also pays a start-up cost of about kStartPages pages); one long request keeps
+  // k = 1, ragged batches whose tiles do not divide evenly over the SMs pick a larger k.
+  // A split keeps at least min_pages pages.
+  const int min_pages = o.min_pages_per_split > 0 ? o.min_pages_per_split : 4;
+  const int max_splits = max_splits_for_merge();
+  constexpr long long kStartPages = 2;
+  long long tile_pages = 0;
+  for (const Group& g : groups) tile_pages += (long long)(g.t1 - g.t0) * g.pages;
+  auto assign = [&](long long T) {
+    for (auto& g : groups) {
+      long long n = o.force_splits > 0 ? o.force_splits : (g.pages + T - 1) / T;
+      g.n_split = (int)std::max<long long>(1, std::min<long long>(std::min<long long>(n, g.pages), max_splits));
+      // pieces of T pages, unless the split count was capped or forced: then equal pieces
+      g.cap = (o.force_splits <= 0 && (long long)g.n_split == (g.pages + T - 1) / T) ? (int)T : 0;
+    }
+  };
+  auto piece_pages = [](const Group& g, int s) {
+    if (g.cap > 0) return std::min(g.pages, (s + 1) * g.cap) - s * g.cap;
+    return (int)((long long)g.pages * (s + 1) / g.n_split - (long long)g.pages * s / g.n_split);
+  };
+  long long best_T = std::max<long long>(min_pages, (tile_pages + num_sms - 1) / num_sms);
+  if (o.force_splits <= 0) {
+    long long best_end = -1;
+    std::vector<long long> lens;
+    for (int k = 1; k <= 4; ++k) {
+      const long long T = std::max<long long>(min_pages, (tile_pages + (long long)num_sms * k - 1) / ((long long)num_sms * k));
+      assign(T);
+      lens.clear();
+      for (const Group& g : groups)
+        for (int s = 0; s < g.n_split; ++s) lens.insert(lens.end(), g.t1 - g.t0, piece_pages(g, s));
+      std::sort(lens.begin(), lens.end(), std::greater<long long>());
+      std::priority_queue<long long, std::vector<long long>, std::greater<long long>> sm;
+      for (int i = 0; i < num_sms; ++i) sm.push(0);
+      long long end = 0;
+      for (long long L : lens) {
+        const long long t = sm.top() + L + kStartPages;
+        sm.pop();
+        sm.push(t);
+        end = std::max(end, t);
+      }
+      if (best_end < 0 || end < best_end) {
+        best_end = end;
+        best_T = T;
+      }
+    }
+  }
+  assign(best_T);
+
+  std::vector<PlanUnit> units;
+  std::vector<PlanMerge> merges;
+  int part_rows = 0;
+  for (const Group& g : groups) {
+    const int b = g.b, n_split = g.n_split, pages = g.pages;
+    std::vector<int> part0(g.t1 - g.t0, -1);
     if (n_split > 1) {
-      for (size_t t = i; t < j; ++t) {
-        part0[t - i] = part_rows;
+      for (size_t t = g.t0; t < g.t1; ++t) {
+        part0[t - g.t0] = part_rows;
         merges.push_back(PlanMerge{tiles[t].qrow0, tiles[t].nrows, part_rows, n_split});
         part_rows += n_split * tiles[t].nrows;
       }
     }
     for (int s = 0; s < n_split; ++s) {
-      int p_begin = (int)((long long)pages * s / n_split), p_end = (int)((long long)pages * (s + 1) / n_split);
+      int p_begin, p_end;
+      if (g.cap > 0) {  // pieces of T = g.cap pages, the last one shorter
+        p_begin = s * g.cap;
+        p_end = std::min(pages, (s + 1) * g.cap);
+      } else {
+        p_begin = (int)((long long)pages * s / n_split);
+        p_end = (int)((long long)pages * (s + 1) / n_split);
+      }
       int kb = p_begin * kPage, ke = std::min(reqs[b].ctx, p_end * kPage);
-      for (size_t t = i; t < j; ++t) {
+      for (size_t t = g.t0; t < g.t1; ++t) {
         PlanUnit u;
         u.b = b; u.qrow0 = tiles[t].qrow0; u.nrows = tiles[t].nrows;
         u.kv_begin = kb; u.kv_end = ke;
-        u.part_row0 = n_split > 1 ? part0[t - i] + s * tiles[t].nrows : -1;
+        u.part_row0 = n_split > 1 ? part0[t - g.t0] + s * tiles[t].nrows : -1;
         u.split = s; u.n_splits = n_split;
         u.ctx = reqs[b].ctx; u.q = reqs[b].q; u.tok0 = reqs[b].tok0; u.reserved = 0;
         units.push_back(u);
       }
     }
-    i = j;
   }
+  // Longest units first: when the grid needs more than one wave, the SMs that finish
+  // early pick up the short units. (Stable, so the tiles of a group stay adjacent.)
+  if ((long long)units.size() > num_sms)
+    std::stable_sort(units.begin(), units.end(), [](const PlanUnit& a, const PlanUnit& c) {
+      return a.kv_end - a.kv_begin > c.kv_end - c.kv_begin;
+    });
 
   size_t req_off = sizeof(PlanHeader);
   size_t units_off = align_up(req_off + sizeof(PlanRequest) * batch, 32);

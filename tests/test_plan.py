@@ -166,3 +166,39 @@ def test_run_rejects_small_workspace_and_foreign_plan():
     bad = plan.copy()
     bad[:4] = 0
     assert _call_run(_run_args(bad, stride=400)) == binding.MLA_ERR_PLAN
+
+
+def _lpt_makespan(lens, num_sms, start_cost=2):
+    """End of an in-order dispatch of units (each SM takes the next unit when free)."""
+    import heapq
+
+    sms = [0] * num_sms
+    for n in lens:
+        t = heapq.heappop(sms)
+        heapq.heappush(sms, t + n + start_cost)
+    return max(sms)
+
+
+@pytest.mark.parametrize("q", [1, 2, 4, 8])
+def test_plan_single_long_request_fits_one_wave(q):
+    """One long request: at most one unit per SM, and no unit much longer than the per-SM
+    share of the tile-pages."""
+    buf, _ = binding.plan([131072], [q], 12, KV, 152)
+    units = read_plan(buf)["units"]
+    assert len(units) <= 152
+    pages = [-(-(u["kv_end"] - u["kv_begin"]) // 64) for u in units]
+    assert max(pages) <= -(-sum(pages) // 152) + 1
+
+
+@pytest.mark.parametrize("H", [48, 96, 128])
+def test_plan_balances_ragged_batches(H):
+    """A ragged batch whose row tiles do not divide evenly over the SMs: units come longest
+    first and an in-order dispatch ends within 15 % of the even share."""
+    g = np.random.default_rng(7 + H)
+    q_lens = g.integers(1, 5, size=32)
+    seq_lens = g.integers(16384, 32769, size=32)
+    buf, _ = binding.plan(seq_lens, q_lens, H, 1, 152)
+    units = read_plan(buf)["units"]
+    pages = [-(-(u["kv_end"] - u["kv_begin"]) // 64) for u in units]
+    assert pages == sorted(pages, reverse=True)
+    assert _lpt_makespan(pages, 152) <= 1.15 * (sum(pages) / 152 + 2)
