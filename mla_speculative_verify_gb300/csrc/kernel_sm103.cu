@@ -776,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // loads is issued before the LSE reduction, so that both wait on memory together.
 constexpr int kMergeThreads = 512;
 constexpr int kMergeWarps = kMergeThreads / 32;
-constexpr int kMergeBatch = 8;  // partial-O loads in flight per lane
+constexpr int kMergeBatch = 10;  // partial-O loads in flight per lane (16 warps x 10 = 160 splits per round trip)
 constexpr int kMergeMaxSplits = 2048;
 
 __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const PlanMerge* merges, const float* part_o,

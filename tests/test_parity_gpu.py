@@ -84,6 +84,15 @@ def test_fp8_query_rows_of_very_different_magnitude():
     _check(prob)
 
 
+@pytest.mark.parametrize("splits", [16, 17, 40])
+@pytest.mark.parametrize("kv", [BF16, FP8])
+def test_both_merge_kernels(splits, kv):
+    """Up to 16 splits per row tile the warp-per-row merge runs, above it the CTA-per-row
+    merge; both against the oracle on a 96-row fold group (two 48-row tiles)."""
+    prob = inputs.make_problem(12, [64 * 45 + 21], [8], kv, seed=2470 + splits, poison_tail=True)
+    _check(prob, PlanOptions(force_splits=splits))
+
+
 def test_many_splits_with_empty_causal_partials():
     """One page per split: the last split holds keys that early verify rows may not see."""
     prob = inputs.make_problem(12, [64 * 6 + 3], [8], BF16, seed=2400, poison_tail=True)
