@@ -350,11 +350,14 @@ def main():
                          hbm_frac=round(gbs / hbm_peak, 3),
                          tensor_frac=round(flops / (ms * 1e-3) / 1e12 / tf_peak, 3),
                          units=c["dec"].info["n_units"], merge_items=c["dec"].info["n_merge"]))
-    # dominant call (largest share of the step): roofline against the measured HBM copy peak
+    # roofline of the dominant kernel (the fold kernel, launched once per call; each timed
+    # call is the whole mla_decode_run, fold + merge): the step's algorithmic bytes over the
+    # step's call time, i.e. per average launch, against the measured HBM copy peak
     dom = int(np.argmax(per_call_ms))
     dprob = res["calls"][dom]["prob"]
-    dbytes = algorithmic_bytes(dprob)
-    achieved = dbytes / (per_call_ms[dom] * 1e-3) / 1e9
+    n_calls = len(res["calls"])
+    dbytes = sum(algorithmic_bytes(c["prob"]) for c in res["calls"]) // n_calls
+    achieved = dbytes / (float(per_call_ms.mean()) * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(us_per_call, 3), "unit": "us/call", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": False, "scaling": "weak",
@@ -371,9 +374,13 @@ def main():
                                                                "kernel_sm103.cu"),
                                                   os.path.join(ROOT, "profiles",
                                                                "fold_decode_kernel_h12_q8_ctx131072_bf16.md"))
-                                 if dprob.name == "h12_q8_ctx131072_bf16" else None),
+                                 if args.workload == "sweep131k" else None),
+                     "traffic_note": "ncu DRAM read+write bytes of one fold launch (the q=8 call; the "
+                                     "other calls read the same cache), from the committed profile when its "
+                                     "kernel source hash matches, else null",
                      "algorithmic_bytes": dbytes,
-                     "kernel": f"fold_decode_kernel + lse_merge_kernel ({dprob.name})",
+                     "kernel": "fold_decode_kernel + lse_merge_kernel, per mla_decode_run call, mean over "
+                               f"the step's {n_calls} calls",
                      "peak_source": f"{peak_src} hbm_gbs"},
         "clocks": res["clocks"],
         "gpu_launches": res["launches"],
