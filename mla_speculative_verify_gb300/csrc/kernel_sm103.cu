@@ -18,25 +18,29 @@
 //
 // One thread issues a tcgen05.mma only every ~60 cycles, while an N = 16..48 MMA
 // needs 20..45 cycles of tensor time, so for a bf16 cache S^T is issued by two warps into
-// two partial accumulators (summed by the softmax) and O^T by a third. For an e4m3 cache
-// S^T takes half the MMAs (K = 32) and multiplies each K step by Q_hi and Q_lo at once
-// (N = 2 nmma), so the two S^T warps take alternate pages. S^T is double-buffered in
-// tensor memory, so the product of the next page runs while the softmax works on this
-// one.
+// two partial accumulators (summed by the softmax), and O^T by four softmax warps (one value
+// block each) as soon as P^T is complete. For an e4m3 cache S^T takes half the MMAs
+// (K = 32) and multiplies each K step by Q_hi and Q_lo at once (N = 2 nmma), so the two S^T
+// warps take alternate pages, and a separate warp issues O^T. S^T is double-buffered in
+// tensor memory, so the product of the next page runs while the softmax works on this one.
 //
 // Warp roles (one CTA per SM):
 //   warp 0     TMA producer: the Q tile once (bf16 cache), then one page per stage
 //              (two bf16 stages, or four e4m3 stages, in the same ring)
 //   warps 1-2  S^T issue (one lane each) into buffer t % 2: bf16 partial p of every
 //              page, or every other page for e4m3
-//   warp 3     O^T issue: the four value blocks of O^T += V^T P^T(t)
-//   warps 4-11 softmax: each thread owns one key of the S^T tile (a TMEM lane) and a
+//   warp 3     e4m3 only: O^T issue, the four value blocks of O^T += V^T P^T(t)
+//   the last 8 softmax: each thread owns one key of the S^T tile (a TMEM lane) and a
 //              quarter of the columns of each 16-column chunk; online
 //              softmax with a lazy per-row reference: the reference moves, and O^T is
 //              rescaled in TMEM, only when a score exceeds it by a few octaves (the
 //              conditional rescale of flashinfer PR #5602); then the epilogue: O / l to
 //              bf16 out and LSE, or fp32 partials for the merge kernel. The eight warps
-//              agree on every decision through OR-reducing named barriers.
+//              agree on every decision through OR-reducing named barriers; for a bf16
+//              cache, after the barrier that closes P^T(t), four of them each issue one
+//              value block of O^T(t) += V^T P^T(t). (On the critical path of the two-stage
+//              bf16 page ring this saves a wake-up and issues the 16 MMAs four at a time;
+//              the e4m3 softmax is already the busiest role, so there a warp does it.)
 //
 // For an e4m3 cache the products run on kind::f8f6f4 MMAs straight from the cached
 // codes: each Q row is scaled by a power of two and split into two e4m3 parts (hi and
@@ -96,10 +100,17 @@ struct Geo {
   static_assert(kStages * kSlot == kKvBytes, "ring size");
 };
 
-constexpr int kMmaWarps = 3;      // two S^T issuers, one O^T issuer
+
 constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, each owning half of the columns
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
-constexpr int kThreads = 32 * (1 + kMmaWarps + kSoftmaxWarps);  // producer, MMA warps, softmax warps
+// Warps: producer, MMA issuers, softmax. bf16: two S^T issuers, and O^T is issued by four
+// of the softmax warps (it is on the critical path of the two-stage page ring). e4m3: two
+// S^T issuers and an O^T warp (the softmax warps are the busiest there).
+template <bool kFp8>
+struct Roles {
+  static constexpr int kMmaWarps = kFp8 ? 3 : 2;
+  static constexpr int kThreads = 32 * (1 + kMmaWarps + kSoftmaxWarps);
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;       // O^T block b at columns 64 b (N <= 64)
 constexpr uint32_t kTmemS = 256;     // S^T buffer b, partial p at columns 256 + 128 b + 64 p
@@ -132,8 +143,8 @@ struct Misc {
   uint64_t bar_q;
   uint64_t kv_full[4], kv_empty[4];
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full[2], pt_empty[2];
-  uint64_t mma_done[4];
+  uint64_t p_full[2], pt_empty[2];  // p_full: e4m3 only (the O^T warp waits on it)
+  uint64_t mma_done[8];
   uint32_t tmem_base;
   int abort;
   int unit[12];  // this CTA's PlanUnit
@@ -212,13 +223,51 @@ __device__ __forceinline__ int sw64_offset(int row, int col) {
   return row * 64 + ((((col >> 4) ^ (row >> 1)) & 3) << 4) + (col & 15);
 }
 
+// O^T += V^T . P^T(t) for value block blk (MN-major V^T from page t's ring slot, MN-major
+// P^T), issued by one lane; accumulates onto the earlier tiles.
+template <bool kFp8>
+__device__ __forceinline__ void issue_ot_block(uint32_t tmem, uint32_t skv, uint32_t spt, int t, int nmma, int blk) {
+  using G = Geo<kFp8>;
+  const uint32_t idesc_o = kFp8 ? ptx::idesc_e4m3(128, nmma, 1, 1) : ptx::idesc_bf16(128, nmma, 1, 1);
+  const uint32_t pt0 = spt + (t & 1) * kPtBytes;
+  // value columns [128 blk, 128 blk + 128) = chunks 2 blk, 2 blk + 1 of the page
+  const uint32_t v0 = skv + (t % G::kStages) * G::kSlot + 2 * blk * G::kChunkBytes;
+  const uint32_t d = tmem + kTmemO + 64 * blk;
+  if constexpr (kFp8) {
+    // K = 32 keys per MMA; P^T = hi + lo parts (64 keys x 64 bytes each)
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        uint64_t ad = ptx::smem_desc(v0 + 2048 * k, G::kChunkBytes, 512, ptx::kSwizzle64B);
+        uint64_t bd = ptx::smem_desc(pt0 + part * (kTileKeys * 64) + 2048 * k, 4096, 512, ptx::kSwizzle64B);
+        ptx::mma_e4m3_ss(d, ad, bd, idesc_o, (t > 0 || k > 0 || part > 0) ? 1u : 0u);
+      }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint64_t ad = ptx::smem_desc(v0 + 2048 * k, G::kChunkBytes, 1024, ptx::kSwizzle128B);
+      uint64_t bd = ptx::smem_desc(pt0 + 2048 * k, 8192, 1024, ptx::kSwizzle128B);
+      ptx::mma_bf16_ss(d, ad, bd, idesc_o, (t > 0 || k > 0) ? 1u : 0u);
+    }
+  }
+}
+
+// Waits (bounded) until the tcgen05 operations this lane issued have completed.
+__device__ __forceinline__ void drain_mmas(uint64_t* done) {
+  ptx::mma_commit(done);
+  long long t0c = clock64();
+  while (!ptx::mbar_try_wait(done, 0) && clock64() - t0c < kWaitBudget) {
+  }
+}
+
 struct SoftmaxArgs {
   Misc* ms;
   uint8_t* sQ;
   uint8_t* sKv;
   uint8_t* sPt;
-  uint32_t tmem;
-  int qd, grp, lane, sidx, b, nrows, qrow0, kv_begin, kv_end, ntiles, part_row0, ctx, qlen, tok0;
+  uint32_t tmem, skv, spt;
+  int qd, grp, lane, sidx, nmma, b, nrows, qrow0, kv_begin, kv_end, ntiles, part_row0, ctx, qlen, tok0;
   volatile int* abort;
 };
 
@@ -227,8 +276,9 @@ struct SoftmaxArgs {
 // 16 columns, the 8 columns 8 grp .. 8 grp + 7: lanes 0..15 read them from TMEM and hand
 // the upper 4 to lanes 16..31, so each thread works on 4 NCH columns of one key: columns
 // 16 c + 8 grp + 4 half + j, c < NCH, j < 4.
+// Returns whether this thread issued O^T MMAs (lane 0 of softmax warps 0..3).
 template <int NCH, bool kFp8>
-__device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params& p) {
+__device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params& p) {
   constexpr int NC = 4 * NCH;
   using G = Geo<kFp8>;
   constexpr float kSlack = kFp8 ? kRefSlackFp8 : kRefSlack;
@@ -238,6 +288,8 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
   const int krow = qd * 16 + (lane & 15);  // key row of this thread in the 64-key tile
   const int col0 = 8 * grp + 4 * half;     // first of this thread's 4 columns in each chunk
   const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+  const int w8 = sidx >> 5;              // softmax warp 0..7; warps 0..3 issue O^T block w8
+  bool issued_ot = false;
   volatile int* abort = a.abort;
   if (sidx == 0 && (p.seq_lens[a.b] != a.ctx || p.q_lens[a.b] != a.qlen)) {
     // the device lengths differ from those the plan was built for: stop the unit
@@ -407,78 +459,102 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
         }
       }
     }
-    if (fail) continue;  // the next tile's vote ends the loop in every warp
     // probabilities relative to the (possibly moved) reference, packed to bf16, or for the
     // e4m3 path times 2^4 and split into hi + lo e4m3 parts
     uint32_t pk[NC / 2];
     uint32_t ph[NCH], pl[NCH];
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      const int n0 = 16 * c + col0;
-      const float4 rr = *reinterpret_cast<const float4*>(&ms->ref[n0]);
-      const float rrv[4] = {rr.x, rr.y, rr.z, rr.w};
-      float pv[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float v = x[4 * c + j];
-        pv[j] = v == -INFINITY ? 0.f : ex2(v - rrv[j]);
-        l_acc[4 * c + j] += pv[j];
-      }
-      if constexpr (kFp8) {
-        const float w0 = pv[0] * kPScaleFp8, w1 = pv[1] * kPScaleFp8, w2 = pv[2] * kPScaleFp8, w3 = pv[3] * kPScaleFp8;
-        const float h0 = round_to_e4m3_precision(w0), h1 = round_to_e4m3_precision(w1);
-        const float h2 = round_to_e4m3_precision(w2), h3 = round_to_e4m3_precision(w3);
-        ph[c] = e4m3x2(h0, h1) | (e4m3x2(h2, h3) << 16);
-        pl[c] = e4m3x2(w0 - h0, w1 - h1) | (e4m3x2(w2 - h2, w3 - h3) << 16);
-      } else {
-        pk[2 * c] = pack_bf16(pv[0], pv[1]);
-        pk[2 * c + 1] = pack_bf16(pv[2], pv[3]);
-      }
-    }
-    if (t >= 2) {
-      fail = !warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p.status);
-      if (fail) continue;
-    }
-    if constexpr (kFp8) {
-      // e4m3 P^T hi and lo, MN-major with 64-byte rows (64-byte swizzle): key krow's row
-      uint8_t* line_hi = a.sPt + sb * kPtBytes + krow * 64;
-      uint8_t* line_lo = line_hi + kTileKeys * 64;
+    if (!fail) {
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
-        const int off = (((c ^ (krow >> 1)) & 3) << 4) + col0;
-        *reinterpret_cast<uint32_t*>(line_hi + off) = ph[c];
-        *reinterpret_cast<uint32_t*>(line_lo + off) = pl[c];
+        const int n0 = 16 * c + col0;
+        const float4 rr = *reinterpret_cast<const float4*>(&ms->ref[n0]);
+        const float rrv[4] = {rr.x, rr.y, rr.z, rr.w};
+        float pv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float v = x[4 * c + j];
+          pv[j] = v == -INFINITY ? 0.f : ex2(v - rrv[j]);
+          l_acc[4 * c + j] += pv[j];
+        }
+        if constexpr (kFp8) {
+          const float w0 = pv[0] * kPScaleFp8, w1 = pv[1] * kPScaleFp8, w2 = pv[2] * kPScaleFp8, w3 = pv[3] * kPScaleFp8;
+          const float h0 = round_to_e4m3_precision(w0), h1 = round_to_e4m3_precision(w1);
+          const float h2 = round_to_e4m3_precision(w2), h3 = round_to_e4m3_precision(w3);
+          ph[c] = e4m3x2(h0, h1) | (e4m3x2(h2, h3) << 16);
+          pl[c] = e4m3x2(w0 - h0, w1 - h1) | (e4m3x2(w2 - h2, w3 - h3) << 16);
+        } else {
+          pk[2 * c] = pack_bf16(pv[0], pv[1]);
+          pk[2 * c + 1] = pack_bf16(pv[2], pv[3]);
+        }
       }
-    } else {
-      uint8_t* line = a.sPt + sb * kPtBytes + krow * 128;
-#pragma unroll
-      for (int c = 0; c < NCH; ++c)
-        *reinterpret_cast<uint2*>(line + ((((2 * c + grp) ^ (krow & 7)) & 7) << 4) + 8 * half) =
-            make_uint2(pk[2 * c], pk[2 * c + 1]);
+      if (t >= 2) fail = !warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p.status);
     }
-    const int key = a.kv_begin + t * kTileKeys + krow;
-    if (key >= a.kv_end) {
-      // a cache slot past the key range: zero its value columns so P = 0 meets V = 0 (this
-      // thread: chunks 2 q4 and 2 q4 + 1, q4 = 2 grp + half)
-      uint8_t* row = a.sKv + (t % G::kStages) * G::kSlot + krow * G::kRowBytes;
-      const int q4 = 2 * grp + half;
+    if (!fail) {
+      if constexpr (kFp8) {
+        // e4m3 P^T hi and lo, MN-major with 64-byte rows (64-byte swizzle): key krow's row
+        uint8_t* line_hi = a.sPt + sb * kPtBytes + krow * 64;
+        uint8_t* line_lo = line_hi + kTileKeys * 64;
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < NCH; ++c) {
+          const int off = (((c ^ (krow >> 1)) & 3) << 4) + col0;
+          *reinterpret_cast<uint32_t*>(line_hi + off) = ph[c];
+          *reinterpret_cast<uint32_t*>(line_lo + off) = pl[c];
+        }
+      } else {
+        uint8_t* line = a.sPt + sb * kPtBytes + krow * 128;
 #pragma unroll
-        for (int j = 0; j < G::kRowBytes / 16; ++j)
-          *reinterpret_cast<uint4*>(row + (2 * q4 + c) * G::kChunkBytes + 16 * j) = make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < NCH; ++c)
+          *reinterpret_cast<uint2*>(line + ((((2 * c + grp) ^ (krow & 7)) & 7) << 4) + 8 * half) =
+              make_uint2(pk[2 * c], pk[2 * c + 1]);
+      }
+      const int key = a.kv_begin + t * kTileKeys + krow;
+      if (key >= a.kv_end) {
+        // a cache slot past the key range: zero its value columns so P = 0 meets V = 0 (this
+        // thread: chunks 2 q4 and 2 q4 + 1, q4 = 2 grp + half)
+        uint8_t* row = a.sKv + (t % G::kStages) * G::kSlot + krow * G::kRowBytes;
+        const int q4 = 2 * grp + half;
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int j = 0; j < G::kRowBytes / 16; ++j)
+            *reinterpret_cast<uint4*>(row + (2 * q4 + c) * G::kChunkBytes + 16 * j) = make_uint4(0, 0, 0, 0);
+      }
+      ptx::fence_async_smem();
+      ptx::tc_fence_before();
     }
-    ptx::fence_async_smem();
-    ptx::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&ms->p_full[sb]);
+    if constexpr (kFp8) {
+      // the O^T warp issues O^T(t) once all softmax warps have arrived; a warp that gave
+      // up a wait leaves the loop with the others at the next tile's vote
+      if (!fail) {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ms->p_full[sb]);
+      }
+      continue;
+    }
+    // P^T(t) is complete once every softmax warp is past this barrier (which also ends the
+    // loop in all warps together if one of them gave up a wait); then warps 0..3 each issue
+    // one value block of O^T(t) and release the page slot and the P^T buffer.
+    if (softmax_any(fail || *abort != 0)) {
+      stop = true;
+      break;
+    }
+    if (w8 < 4) {
+      ptx::tc_fence_after();
+      if (lane == 0) {
+        issue_ot_block<kFp8>(a.tmem, a.skv, a.spt, t, a.nmma, w8);
+        ptx::mma_commit(&ms->kv_empty[t % G::kStages]);
+        ptx::mma_commit(&ms->pt_empty[sb]);
+        issued_ot = true;
+      }
+      __syncwarp();
+    }
   }
   // ------------------------------------------------------------ epilogue
   if (!stop) {
     if (!fail) fail = !warp_wait(&ms->pt_empty[(a.ntiles - 1) & 1], ((a.ntiles - 1) >> 1) & 1, abort, p.status);
     stop = softmax_any(fail || *abort != 0);
   }
-  if (stop) return;
+  if (stop) return issued_ot;
   ptx::tc_fence_after();
 #pragma unroll
   for (int i = 0; i < NC; ++i) {
@@ -522,10 +598,11 @@ __device__ __forceinline__ void softmax_role(const SoftmaxArgs& a, const Params&
       }
     }
   }
+  return issued_ot;
 }
 
 template <bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
     fold_decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv, Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base (the 128-byte swizzle atoms), kept in the shared window
@@ -553,15 +630,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&ms->bar_q, kFp8 ? kSoftmaxWarps : 1);  // e4m3: the softmax warps convert Q themselves
     for (int i = 0; i < 4; ++i) {
       ptx::mbar_init(&ms->kv_full[i], 1);
-      ptx::mbar_init(&ms->kv_empty[i], 1);  // the O^T warp
+      ptx::mbar_init(&ms->kv_empty[i], kFp8 ? 1 : 4);  // the O^T issuer(s)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&ms->s_full[i], kFp8 ? 1 : 2);  // the S^T warp(s) of a tile
       ptx::mbar_init(&ms->s_empty[i], kSoftmaxWarps);
+      ptx::mbar_init(&ms->pt_empty[i], kFp8 ? 1 : 4);
       ptx::mbar_init(&ms->p_full[i], kSoftmaxWarps);
-      ptx::mbar_init(&ms->pt_empty[i], 1);  // the O^T warp
     }
-    for (int i = 0; i < 4; ++i) ptx::mbar_init(&ms->mma_done[i], 1);
+    for (int i = 0; i < 8; ++i) ptx::mbar_init(&ms->mma_done[i], 1);
     ptx::fence_mbar_init();
     }
     int uw = 0;
@@ -651,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp <= kMmaWarps) {
+  } else if (warp <= Roles<kFp8>::kMmaWarps) {
     // ------------------------------------------------------------ MMA issue
     const uint32_t sq = ptx::smem_addr(sQ), skv = ptx::smem_addr(sKv), spt = ptx::smem_addr(sPt);
     bool ok = !*abort && warp_wait(&ms->bar_q, 0, abort, p.status);
@@ -696,41 +773,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         issued = true;
       }
-    } else {
-      // O^T += V^T . P^T(t) (MN-major V^T, MN-major P^T), all four value blocks
-      const uint32_t idesc_o = kFp8 ? ptx::idesc_e4m3(128, nmma, 1, 1) : ptx::idesc_bf16(128, nmma, 1, 1);
+    }
+    if (kFp8 && warp == 3) {
+      // e4m3: O^T(t) += V^T . P^T(t), all four value blocks, once the softmax warps have
+      // written P^T(t)
       for (int t = 0; ok && t < ntiles; ++t) {
         ok = warp_wait(&ms->p_full[t & 1], (t >> 1) & 1, abort, p.status);
         if (!ok) break;
         ptx::tc_fence_after();
         if (lane == 0) {
-          const int slot = t % S;
-          const uint32_t pt0 = spt + (t & 1) * kPtBytes;
 #pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
-            // value columns [128 blk, 128 blk + 128) = chunks 2 blk, 2 blk + 1 of the page
-            const uint32_t v0 = skv + slot * G::kSlot + 2 * blk * G::kChunkBytes;
-            const uint32_t d = tmem + kTmemO + 64 * blk;
-            if constexpr (kFp8) {
-              // K = 32 keys per MMA; P^T = hi + lo parts (64 keys x 64 bytes each)
-#pragma unroll
-              for (int k = 0; k < 2; ++k)
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                  uint64_t ad = ptx::smem_desc(v0 + 2048 * k, G::kChunkBytes, 512, ptx::kSwizzle64B);
-                  uint64_t bd = ptx::smem_desc(pt0 + part * (kTileKeys * 64) + 2048 * k, 4096, 512, ptx::kSwizzle64B);
-                  ptx::mma_e4m3_ss(d, ad, bd, idesc_o, (t > 0 || k > 0 || part > 0) ? 1u : 0u);
-                }
-            } else {
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                uint64_t ad = ptx::smem_desc(v0 + 2048 * k, G::kChunkBytes, 1024, ptx::kSwizzle128B);
-                uint64_t bd = ptx::smem_desc(pt0 + 2048 * k, 8192, 1024, ptx::kSwizzle128B);
-                ptx::mma_bf16_ss(d, ad, bd, idesc_o, (t > 0 || k > 0) ? 1u : 0u);
-              }
-            }
-          }
-          ptx::mma_commit(&ms->kv_empty[slot]);
+          for (int blk = 0; blk < 4; ++blk) issue_ot_block<kFp8>(tmem, skv, spt, t, nmma, blk);
+          ptx::mma_commit(&ms->kv_empty[t % S]);
           ptx::mma_commit(&ms->pt_empty[t & 1]);
         }
         __syncwarp();
@@ -739,26 +793,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // every MMA this warp issued must retire before TMEM is released
     if (issued) {
-      if (lane == 0) {
-        uint64_t* done = &ms->mma_done[warp - 1];
-        ptx::mma_commit(done);
-        long long t0c = clock64();
-        while (!ptx::mbar_try_wait(done, 0) && clock64() - t0c < kWaitBudget) {
-        }
-      }
+      if (lane == 0) drain_mmas(&ms->mma_done[warp - 1]);
       __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const SoftmaxArgs a{ms, sQ, sKv, sPt, tmem, warp & 3, (warp - 1 - kMmaWarps) >> 2, lane,
-                        tid - 32 * (kMmaWarps + 1), b, nrows, qrow0, kv_begin, kv_end,
-                        ntiles, part_row0, ctx, qlen, tok0, abort};
+    constexpr int kMma = Roles<kFp8>::kMmaWarps;
+    const SoftmaxArgs a{ms, sQ, sKv, sPt, tmem, ptx::smem_addr(sKv), ptx::smem_addr(sPt), warp & 3,
+                        (warp - 1 - kMma) >> 2, lane, tid - 32 * (kMma + 1), nmma, b, nrows, qrow0,
+                        kv_begin, kv_end, ntiles, part_row0, ctx, qlen, tok0, abort};
+    bool issued_ot;
     if (nch == 1)
-      softmax_role<1, kFp8>(a, p);
+      issued_ot = softmax_role<1, kFp8>(a, p);
     else if (nch == 2)
-      softmax_role<2, kFp8>(a, p);
+      issued_ot = softmax_role<2, kFp8>(a, p);
     else
-      softmax_role<3, kFp8>(a, p);
+      issued_ot = softmax_role<3, kFp8>(a, p);
+    // the O^T MMAs this lane issued must retire before TMEM is released
+    if (issued_ot) drain_mmas(&ms->mma_done[3 + (warp - 1 - kMma)]);
+    __syncwarp();
   }
 
   ptx::tc_fence_before();
@@ -1054,9 +1107,9 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
   prm.status = status_dev;
   cudaStream_t st = (cudaStream_t)stream;
   if (fp8)
-    fold_decode_kernel<true><<<h->n_units, kThreads, kSmemBytes, st>>>(tq, tkv, prm);
+    fold_decode_kernel<true><<<h->n_units, Roles<true>::kThreads, kSmemBytes, st>>>(tq, tkv, prm);
   else
-    fold_decode_kernel<false><<<h->n_units, kThreads, kSmemBytes, st>>>(tq, tkv, prm);
+    fold_decode_kernel<false><<<h->n_units, Roles<false>::kThreads, kSmemBytes, st>>>(tq, tkv, prm);
   ce = cudaGetLastError();
   if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "fold kernel launch: %s", cudaGetErrorString(ce));
   if (h->n_merge > 0) {
