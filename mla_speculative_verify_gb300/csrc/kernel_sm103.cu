@@ -218,6 +218,18 @@ __device__ __forceinline__ float round_to_e4m3_precision(float x) {
 __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
+// Two fp32 values (<= 448) -> hi and lo e4m3 pairs with hi + lo ~ the values: through f16x2
+// (11 significant bits, more than hi + lo keep), hi = the e4m3 rounding, lo = the e4m3
+// rounding of the f16 remainder. Each result holds the first value in its low byte.
+__device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 w = __floats2half2_rn(a, b);
+  const __nv_fp8x2_storage_t h = __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&w), __NV_SATFINITE,
+                                                           __NV_E4M3);
+  const __half2_raw hb = __nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3);
+  const __half2 r = __hsub2(w, *reinterpret_cast<const __half2*>(&hb));
+  hi = (uint32_t)h;
+  lo = (uint32_t)__nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&r), __NV_SATFINITE, __NV_E4M3);
+}
 // Byte offset of (row, column) in a 64-byte-swizzled e4m3 region with 64-byte rows.
 __device__ __forceinline__ int sw64_offset(int row, int col) {
   return row * 64 + ((((col >> 4) ^ (row >> 1)) & 3) << 4) + (col & 15);
@@ -477,11 +489,11 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
           l_acc[4 * c + j] += pv[j];
         }
         if constexpr (kFp8) {
-          const float w0 = pv[0] * kPScaleFp8, w1 = pv[1] * kPScaleFp8, w2 = pv[2] * kPScaleFp8, w3 = pv[3] * kPScaleFp8;
-          const float h0 = round_to_e4m3_precision(w0), h1 = round_to_e4m3_precision(w1);
-          const float h2 = round_to_e4m3_precision(w2), h3 = round_to_e4m3_precision(w3);
-          ph[c] = e4m3x2(h0, h1) | (e4m3x2(h2, h3) << 16);
-          pl[c] = e4m3x2(w0 - h0, w1 - h1) | (e4m3x2(w2 - h2, w3 - h3) << 16);
+          uint32_t h01, l01, h23, l23;
+          split_e4m3x2(pv[0] * kPScaleFp8, pv[1] * kPScaleFp8, h01, l01);
+          split_e4m3x2(pv[2] * kPScaleFp8, pv[3] * kPScaleFp8, h23, l23);
+          ph[c] = h01 | (h23 << 16);
+          pl[c] = l01 | (l23 << 16);
         } else {
           pk[2 * c] = pack_bf16(pv[0], pv[1]);
           pk[2 * c + 1] = pack_bf16(pv[2], pv[3]);
