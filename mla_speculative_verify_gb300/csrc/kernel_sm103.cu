@@ -117,9 +117,11 @@ constexpr uint32_t kTmemS = 256;     // S^T buffer b, partial p at columns 256 +
 constexpr float kRefSlack = 8.0f;    // octaves a score may exceed the row reference before it moves
 // e4m3 path: a smaller slack (p <= 16) so that P can be stored times 2^4 (<= 256 < 448,
 // the largest e4m3); probabilities down to 2^-10 of the reference stay in e4m3's normal
-// range, smaller ones keep an absolute error below 2^-14
+// range, smaller ones keep an absolute error below 2^-14. The 2^4 is applied by keeping
+// the stored reference kPShiftFp8 octaves below the row's reference, so exp2(s - ref) is
+// already P times 2^4; l carries the same factor, which cancels in O / l and in the LSE.
 constexpr float kRefSlackFp8 = 4.0f;
-constexpr float kPScaleFp8 = 16.0f;
+constexpr float kPShiftFp8 = 4.0f;
 constexpr long long kWaitBudget = 2000000000LL;  // cycles (~1 s) before a wait gives up
 
 struct Params {
@@ -293,7 +295,8 @@ template <int NCH, bool kFp8>
 __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params& p) {
   constexpr int NC = 4 * NCH;
   using G = Geo<kFp8>;
-  constexpr float kSlack = kFp8 ? kRefSlackFp8 : kRefSlack;
+  constexpr float kPShift = kFp8 ? kPShiftFp8 : 0.f;
+  constexpr float kMoveAbove = (kFp8 ? kRefSlackFp8 : kRefSlack) + kPShift;  // score - stored ref
   Misc* ms = a.ms;
   const int lane = a.lane, qd = a.qd, grp = a.grp, sidx = a.sidx;
   const int half = lane >> 4;
@@ -376,6 +379,7 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
     const int sb = t & 1;
     float x[NC];
     bool need = false;
+    bool unmasked = false;  // this tile: every key visible to every row
     if (!fail) fail = !warp_wait(&ms->s_full[sb], (t >> 1) & 1, abort, p.status);
     if (!fail) {
       ptx::tc_fence_after();
@@ -402,7 +406,7 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
       if (lane == 0) ptx::mbar_arrive(&ms->s_empty[sb]);
       const int key = a.kv_begin + t * kTileKeys + krow;
       const int tile_last = a.kv_begin + t * kTileKeys + kTileKeys - 1;
-      const bool unmasked = tile_last < a.kv_end && tile_last < lim_min;  // tile-uniform fast path
+      unmasked = tile_last < a.kv_end && tile_last < lim_min;  // tile-uniform fast path
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         const int n0 = 16 * c + col0;
@@ -416,7 +420,7 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
           float v = x[4 * c + j] * csv[j];
           if (!unmasked) v = (key < a.kv_end && key < ms->lim[n0 + j]) ? v : -INFINITY;
           x[4 * c + j] = v;
-          need |= v > rrv[j] + kSlack;
+          need |= v > rrv[j] + kMoveAbove;
         }
       }
     }
@@ -438,7 +442,7 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
       if (sidx < 16 * NCH) {
         const float cm = fmaxf(fmaxf(ms->colred[0][sidx], ms->colred[1][sidx]), fmaxf(ms->colred[2][sidx], ms->colred[3][sidx]));
         const float old = ms->ref[sidx];
-        const float nw = fmaxf(old, cm);
+        const float nw = fmaxf(old, cm - kPShift);
         ms->alpha[sidx] = (nw == old) ? 1.f : ex2(old - nw);
         ms->ref[sidx] = nw;
       }
@@ -482,16 +486,22 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
         const float4 rr = *reinterpret_cast<const float4*>(&ms->ref[n0]);
         const float rrv[4] = {rr.x, rr.y, rr.z, rr.w};
         float pv[4];
+        if (unmasked) {  // no masked score, and every row's reference is finite
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float v = x[4 * c + j];
-          pv[j] = v == -INFINITY ? 0.f : ex2(v - rrv[j]);
-          l_acc[4 * c + j] += pv[j];
+          for (int j = 0; j < 4; ++j) pv[j] = ex2(x[4 * c + j] - rrv[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float v = x[4 * c + j];
+            pv[j] = v == -INFINITY ? 0.f : ex2(v - rrv[j]);
+          }
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) l_acc[4 * c + j] += pv[j];
         if constexpr (kFp8) {
           uint32_t h01, l01, h23, l23;
-          split_e4m3x2(pv[0] * kPScaleFp8, pv[1] * kPScaleFp8, h01, l01);
-          split_e4m3x2(pv[2] * kPScaleFp8, pv[3] * kPScaleFp8, h23, l23);
+          split_e4m3x2(pv[0], pv[1], h01, l01);
+          split_e4m3x2(pv[2], pv[3], h23, l23);
           ph[c] = h01 | (h23 << 16);
           pl[c] = l01 | (l23 << 16);
         } else {
@@ -1110,7 +1120,7 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
   prm.q_lens = q_lens;
   const float ks = fp8 ? kv_scale : 1.0f;
   prm.score_scale_log2 = sm_scale * ks * 1.4426950408889634f;
-  prm.out_scale = fp8 ? ks / kPScaleFp8 : ks;  // the e4m3 path accumulates P times 2^4
+  prm.out_scale = ks;
   prm.out = (__nv_bfloat16*)out;
   prm.lse = lse;
   prm.part_o = (float*)workspace;
