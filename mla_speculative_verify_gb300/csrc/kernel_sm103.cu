@@ -154,7 +154,7 @@ struct Misc {
   alignas(16) float alpha[64];
   alignas(16) int lim[64];
   alignas(16) float colred[4][64];  // per TMEM lane quadrant, per packed row
-  alignas(16) float lsum[64];
+  alignas(16) float oscale[64];  // per packed row: output scale / l (0 for padding rows)
   alignas(16) float colscale[64];  // e4m3 path: score scale of each row (its Q split scale folded in)
 };
 static_assert(offsetof(Misc, ref) % 16 == 0, "float4 reads of ref need 16-byte alignment");
@@ -326,21 +326,26 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
     // K Q_lo^T. Row r is scaled by 2^e_r so that its largest |q| lands in [128, 256);
     // hi = q 2^e_r rounded to e4m3, lo = the remainder in e4m3: hi + lo reproduces the
     // bf16 row to ~2^-17 of its largest entry. 2^-e_r goes into the row's score scale.
+    // This warp's rows r = w8 + 8 k: all of their loads go out first (one round trip).
     const float base = p.score_scale_log2;
-    for (int r = (sidx >> 5); r < 16 * NCH; r += kSoftmaxWarps) {
-      const int grow = a.qrow0 + r;
+    constexpr int kRowsPerWarp = 16 * NCH / kSoftmaxWarps;
+    uint32_t raw[kRowsPerWarp][9];
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      const int grow = a.qrow0 + w8 + kSoftmaxWarps * k;
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(p.q + (size_t)grow * kDqk + 18 * lane);
+#pragma unroll
+      for (int j = 0; j < 9; ++j) raw[k][j] = grow < p.q_rows ? src[j] : 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      const int r = w8 + kSoftmaxWarps * k;
       float v[18];
-      if (grow < p.q_rows) {
-        const __nv_bfloat162* src = reinterpret_cast<const __nv_bfloat162*>(p.q + (size_t)grow * kDqk + 18 * lane);
 #pragma unroll
-        for (int j = 0; j < 9; ++j) {
-          const float2 f = __bfloat1622float2(src[j]);
-          v[2 * j] = f.x;
-          v[2 * j + 1] = f.y;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 18; ++j) v[j] = 0.f;
+      for (int j = 0; j < 9; ++j) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[k][j]));
+        v[2 * j] = f.x;
+        v[2 * j + 1] = f.y;
       }
       float mx = 0.f;
 #pragma unroll
@@ -586,36 +591,45 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
     if ((lane & 15) == 0) ms->colred[qd][16 * (i / 4) + col0 + (i % 4)] = s;
   }
   softmax_sync();
-  if (sidx < a.nrows) {
-    const float L = ms->colred[0][sidx] + ms->colred[1][sidx] + ms->colred[2][sidx] + ms->colred[3][sidx];
-    ms->lsum[sidx] = L;
-    const float lse_v = L > 0.f ? (ms->ref[sidx] + lg2(L)) * 0.69314718055994531f : -INFINITY;
-    if (a.part_row0 < 0) {
-      if (p.lse) p.lse[a.qrow0 + sidx] = lse_v;
-    } else {
-      p.part_lse[a.part_row0 + sidx] = lse_v;
+  if (sidx < 64) {
+    float L = 0.f;
+    if (sidx < a.nrows) {
+      L = ms->colred[0][sidx] + ms->colred[1][sidx] + ms->colred[2][sidx] + ms->colred[3][sidx];
+      const float lse_v = L > 0.f ? (ms->ref[sidx] + lg2(L)) * 0.69314718055994531f : -INFINITY;
+      if (a.part_row0 < 0) {
+        if (p.lse) p.lse[a.qrow0 + sidx] = lse_v;
+      } else {
+        p.part_lse[a.part_row0 + sidx] = lse_v;
+      }
     }
+    ms->oscale[sidx] = L > 0.f ? p.out_scale / L : 0.f;  // one division per row
   }
   softmax_sync();
+  // O^T(dv, row) / l(row): this thread holds dv = 128 blk + 32 qd + lane of value blocks
+  // 2 grp, 2 grp + 1; a warp's stores of one row cover 32 consecutive dv
   const int dv_in_blk = qd * 32 + lane;
 #pragma unroll 1
   for (int blk = 2 * grp; blk < 2 * grp + 2; ++blk) {
     const int dv = blk * 128 + dv_in_blk;
+    float o[NCH][16];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) ptx::tmem_ld16(a.tmem + kTmemO + 64 * blk + lane_off + 16 * c, o[c]);
+    ptx::tmem_ld_wait();
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
-      float o[16];
-      ptx::tmem_ld16(a.tmem + kTmemO + 64 * blk + lane_off + 16 * c, o);
-      ptx::tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int n = 16 * c + j;
-        if (n < a.nrows) {
-          const float L = ms->lsum[n];
-          const float v = L > 0.f ? o[j] * (p.out_scale / L) : 0.f;
-          if (a.part_row0 < 0)
-            p.out[(size_t)(a.qrow0 + n) * kDv + dv] = __float2bfloat16_rn(v);
-          else
-            p.part_o[(size_t)(a.part_row0 + n) * kDv + dv] = v;
+      for (int j = 0; j < 16; j += 4) {
+        const float4 sc = *reinterpret_cast<const float4*>(&ms->oscale[16 * c + j]);
+        const float v4[4] = {o[c][j] * sc.x, o[c][j + 1] * sc.y, o[c][j + 2] * sc.z, o[c][j + 3] * sc.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int n = 16 * c + j + u;
+          if (n < a.nrows) {
+            if (a.part_row0 < 0)
+              p.out[(size_t)(a.qrow0 + n) * kDv + dv] = __float2bfloat16_rn(v4[u]);
+            else
+              p.part_o[(size_t)(a.part_row0 + n) * kDv + dv] = v4[u];
+          }
         }
       }
     }
