@@ -57,6 +57,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "mla_decode.h"
@@ -859,8 +860,9 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
 }
 
 // ------------------------------------------------------------------ LSE merge
-// One CTA per (packed row, quarter of the 512 value columns): 16 warps share the
-// splits of the row. L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s; a split that
+// One CTA per (packed row, quarter of the 512 value columns): its W warps (4, 8 or 16,
+// enough for all splits at kMergeBatch loads per lane) share the splits of the row; fewer
+// warps per CTA let more CTAs share an SM. L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s; a split that
 // a causal row cannot see has L_s = -inf and weight 0. The first batch of partial-O
 // loads is issued before the LSE reduction, so that both wait on memory together.
 constexpr int kMergeThreads = 512;
@@ -868,16 +870,18 @@ constexpr int kMergeWarps = kMergeThreads / 32;
 constexpr int kMergeBatch = 10;  // partial-O loads in flight per lane (16 warps x 10 = 160 splits per round trip)
 constexpr int kMergeMaxSplits = 2048;
 
-__global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const PlanMerge* merges, const float* part_o,
+template <int W>
+__global__ void __launch_bounds__(32 * W) lse_merge_kernel(const PlanMerge* merges, const float* part_o,
                                                                  const float* part_lse, __nv_bfloat16* out, float* lse) {
   ptx::pdl_wait_primary();
   __shared__ float w_s[kMergeMaxSplits];
-  __shared__ float red[kMergeWarps][2];
-  __shared__ float4 acc_s[kMergeWarps][32];
+  __shared__ float red[W][2];
+  __shared__ float4 acc_s[W][32];
   const PlanMerge m = merges[blockIdx.y];
   const int row = blockIdx.x >> 2, quarter = blockIdx.x & 3;
   if (row >= m.nrows) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int nw = W, nt = 32 * W;  // warps: chosen by the host for the split count
   const int ns = m.n_splits;  // the planner keeps this <= kMergeMaxSplits
   const int col = quarter * 128 + 4 * lane;
   const float* base = part_o + (size_t)(m.part_row0 + row) * kDv + col;
@@ -885,12 +889,12 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const PlanMerg
   float4 v[kMergeBatch];
 #pragma unroll
   for (int u = 0; u < kMergeBatch; ++u) {
-    const int s = warp + kMergeWarps * u;
+    const int s = warp + nw * u;
     v[u] = s < ns ? __ldcs(reinterpret_cast<const float4*>(base + (size_t)s * split_stride)) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   // 1. L over the splits
   float mx = -INFINITY;
-  for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
+  for (int s = threadIdx.x; s < ns; s += nt) {
     const float x = part_lse[m.part_row0 + s * m.nrows + row];
     w_s[s] = x;
     mx = fmaxf(mx, x);
@@ -901,9 +905,9 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const PlanMerg
   __syncthreads();
   mx = red[0][0];
 #pragma unroll
-  for (int i = 1; i < kMergeWarps; ++i) mx = fmaxf(mx, red[i][0]);
+  for (int i = 1; i < W; ++i) mx = fmaxf(mx, red[i][0]);
   float sum = 0.f;
-  for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
+  for (int s = threadIdx.x; s < ns; s += nt) {
     const float x = w_s[s];
     sum += x == -INFINITY ? 0.f : __expf(x - mx);
   }
@@ -913,9 +917,9 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const PlanMerg
   __syncthreads();
   sum = 0.f;
 #pragma unroll
-  for (int i = 0; i < kMergeWarps; ++i) sum += red[i][1];
+  for (int i = 0; i < W; ++i) sum += red[i][1];
   const float L = mx + __logf(sum);
-  for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
+  for (int s = threadIdx.x; s < ns; s += nt) {
     const float x = w_s[s];
     w_s[s] = x == -INFINITY ? 0.f : __expf(x - L);
   }
@@ -925,17 +929,17 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const PlanMerg
   for (int s0 = 0;;) {
 #pragma unroll
     for (int u = 0; u < kMergeBatch; ++u) {
-      const int s = s0 + warp + kMergeWarps * u;
+      const int s = s0 + warp + nw * u;
       if (s < ns) {
         const float w = w_s[s];
         acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;
       }
     }
-    s0 += kMergeWarps * kMergeBatch;
+    s0 += nw * kMergeBatch;
     if (s0 >= ns) break;
 #pragma unroll
     for (int u = 0; u < kMergeBatch; ++u) {
-      const int s = s0 + warp + kMergeWarps * u;
+      const int s = s0 + warp + nw * u;
       v[u] = s < ns ? __ldcs(reinterpret_cast<const float4*>(base + (size_t)s * split_stride))
                     : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -945,7 +949,7 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const PlanMerg
   if (warp == 0) {
     float4 r = acc_s[0][lane];
 #pragma unroll
-    for (int i = 1; i < kMergeWarps; ++i) {
+    for (int i = 1; i < W; ++i) {
       const float4 x = acc_s[i][lane];
       r.x += x.x; r.y += x.y; r.z += x.z; r.w += x.w;
     }
@@ -1157,7 +1161,10 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = small ? dim3((unsigned)((h->rows_cap * 4 + kMergeSmallWarps - 1) / kMergeSmallWarps), (unsigned)h->n_merge, 1)
                         : dim3((unsigned)(h->rows_cap * 4), (unsigned)h->n_merge, 1);
-    cfg.blockDim = dim3(small ? 32 * kMergeSmallWarps : kMergeThreads, 1, 1);
+    // CTA-per-row merge: just enough warps for one round trip of loads (fewer registers per
+    // CTA, so more of them fit on an SM as the fold kernel's CTAs leave)
+    const int large_warps = max_ns <= 4 * kMergeBatch ? 4 : max_ns <= 8 * kMergeBatch ? 8 : kMergeWarps;
+    cfg.blockDim = dim3(small ? 32 * kMergeSmallWarps : 32 * large_warps, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1165,7 +1172,10 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    ce = cudaLaunchKernelEx(&cfg, small ? lse_merge_small_kernel : lse_merge_kernel,
+    ce = cudaLaunchKernelEx(&cfg,
+                            small ? lse_merge_small_kernel
+                                  : large_warps == 4 ? lse_merge_kernel<4>
+                                                     : large_warps == 8 ? lse_merge_kernel<8> : lse_merge_kernel<kMergeWarps>,
                             (const PlanMerge*)((const uint8_t*)plan_dev + h->merge_off), (const float*)prm.part_o,
                             (const float*)prm.part_lse, (__nv_bfloat16*)out, lse);
     if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "merge kernel launch: %s", cudaGetErrorString(ce));
