@@ -718,8 +718,10 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
     {
       const int32_t* pt_row = p.page_table + (size_t)b * p.pt_stride + kv_begin / kPage;
       // page ids 32 at a time (one per lane), the next batch read one batch ahead. An id
-      // outside the cache is reported and replaced by page 0. (Prefetching pages into L2
-      // ahead of the ring measured slower: the extra requests queue in front of the loads.)
+      // outside the cache is reported and replaced by page 0. With the copy of page t the
+      // producer also asks L2 for page t + S, the next one to enter the ring, so that its
+      // copy (issued once O^T(t) frees the slot) is served by L2. (Prefetching four pages
+      // beyond the ring measured slower: those requests queue in front of the ring's own.)
       auto checked = [&](int pid, int t) {
         if (t < ntiles && (pid < 0 || pid >= p.num_pages)) {
           report(p.status, MLA_DEVICE_BAD_PAGE);
@@ -734,6 +736,8 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
         const int cnt = min(32, ntiles - t0);
         for (int i = 0; i < cnt; ++i) {
           const int page = __shfl_sync(0xffffffffu, pid_cur, i);
+          const int tp = i + S;  // the page after the ring (index relative to t0)
+          const int page_pf = __shfl_sync(0xffffffffu, tp < 32 ? pid_cur : pid_next, tp & 31);
           const int t = t0 + i, slot = t % S;
           int ok = 1;
           if (lane == 0) {
@@ -741,6 +745,7 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
             if (ok) {
               ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], G::kSlot);
               ptx::tma_load_3d(sKv + slot * G::kSlot, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0);
+              if (t0 + tp < ntiles) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, page_pf * kPage, 0);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
