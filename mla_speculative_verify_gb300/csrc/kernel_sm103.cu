@@ -26,12 +26,14 @@
 //
 // Warp roles (one CTA per SM):
 //   warp 0     TMA producer: the Q tile once (bf16 cache), then one page per stage
-//              (two bf16 stages, or four e4m3 stages, in the same ring)
+//              (two bf16 stages, or four e4m3 stages, in the same ring), each copy with
+//              an L2 prefetch of the page that enters the ring next
 //   warps 1-2  S^T issue (one lane each) into buffer t % 2: bf16 partial p of every
 //              page, or every other page for e4m3
 //   warp 3     e4m3 only: O^T issue, the four value blocks of O^T += V^T P^T(t)
-//   the last 8 softmax: each thread owns one key of the S^T tile (a TMEM lane) and a
-//              quarter of the columns of each 16-column chunk; online
+//   8 softmax warps (3-10 for bf16, 4-11 for e4m3): each thread owns one key of the
+//              S^T tile (a TMEM lane) and a quarter of the columns of each 16-column
+//              chunk; online
 //              softmax with a lazy per-row reference: the reference moves, and O^T is
 //              rescaled in TMEM, only when a score exceeds it by a few octaves (the
 //              conditional rescale of flashinfer PR #5602); then the epilogue: O / l to
