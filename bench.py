@@ -8,10 +8,14 @@ per call in microseconds; the KV bandwidth and the roofline fraction go beside i
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                         [--workload sweep131k|long_bf16|long_fp8|h96|ragged48|ragged128]
 
-Timing: each call runs as a CUDA-graph replay, bracketed by CUDA events on the
-stream it runs on. Every call of a step reads its own cache, and the step's caches
-together are several times the 126 MB L2, so no call finds its cache in L2; with
---l2 flush a 256 MB write before every timed call also evicts everything else.
+Timing: each call is captured R times back to back (--graph-calls, default 4) in one
+CUDA graph, every copy reading a cache of its own, and the graph replay is bracketed by
+CUDA events on the stream it runs on; time per call = graph time / R. (A serving engine
+replays the whole decode step as one graph, so this leaves out the per-graph launch gap
+of a graph that holds a single call.) Every call reads a cache that no call since it
+was last read has left in L2: the R copies of a call and the calls of a step together
+are many times the 126 MB L2. With --l2 flush a 256 MB write before every graph replay
+also evicts everything else.
 SM clocks and throttle reasons are sampled with nvidia-smi during the timed region.
 """
 from __future__ import annotations
@@ -165,10 +169,12 @@ def run_ours(args, probs, desc, rank, world):
     stream = torch.cuda.Stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     calls = []
+    R = args.graph_calls
     for prob in probs:
         dec = VerifyDecoder(prob.seq_lens, prob.q_lens, prob.H, prob.kv_dtype, dev)
         q = prob.q.to(dev)
         kv = prob.kv.to(dev)
+        kvs = [kv] + [kv.clone() for _ in range(R - 1)]  # a cache of its own for every copy of the call
         pt = torch.from_numpy(prob.page_table).to(dev)
         out = torch.empty((prob.total_q, prob.H, 512), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((prob.total_q, prob.H), dtype=torch.float32, device=dev)
@@ -179,9 +185,10 @@ def run_ours(args, probs, desc, rank, world):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream):
-                dec.run(q, kv, pt, out, lse, prob.sm_scale, prob.kv_scale, status)
-        calls.append(dict(prob=prob, dec=dec, q=q, kv=kv, pt=pt, out=out, lse=lse, status=status, graph=g))
-    launches_per_step = sum(1 + (1 if c["dec"].info["n_merge"] > 0 else 0) for c in calls)
+                for r in range(R):
+                    dec.run(q, kvs[r], pt, out, lse, prob.sm_scale, prob.kv_scale, status)
+        calls.append(dict(prob=prob, dec=dec, q=q, kv=kv, kvs=kvs, pt=pt, out=out, lse=lse, status=status, graph=g))
+    launches_per_step = R * sum(1 + (1 if c["dec"].info["n_merge"] > 0 else 0) for c in calls)
 
     def one_step(timed: bool):
         evs = []
@@ -212,8 +219,9 @@ def run_ours(args, probs, desc, rank, world):
         wall = time.perf_counter() - t0
     if world > 1:
         torch.distributed.barrier()
-    per_call_ms = np.array([[e0.elapsed_time(e1) for (e0, e1) in evs] for evs in all_evs])  # [K, calls]
-    step_ms = per_call_ms.sum(1)
+    graph_ms = np.array([[e0.elapsed_time(e1) for (e0, e1) in evs] for evs in all_evs])  # [K, calls]
+    step_ms = graph_ms.sum(1)  # a step replays every call's graph: R calls of each
+    per_call_ms = graph_ms / R
     status_bits = 0
     for c in calls:
         status_bits |= int(c["status"].item())
@@ -296,6 +304,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="sweep131k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph-calls", type=int, default=4, choices=range(1, 65), metavar="1..64",
+                    help="copies of each call, each on a cache of its own, captured back to back in the call's "
+                         "CUDA graph (time per call = graph time / this)")
     ap.add_argument("--l2", default="none", choices=["flush", "none"],
                     help="none (default): rely on the step's inputs being larger than L2 (every call of a "
                          "step reads its own cache of >= 151 MB, all of them together >= 604 MB); flush: "
@@ -337,7 +348,7 @@ def main():
         t = torch.tensor([step_ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         step_ms = float(t.item())
-    us_per_call = step_ms * 1000.0 / calls_per_step
+    us_per_call = step_ms * 1000.0 / (calls_per_step * args.graph_calls)
     hbm_peak, tf_peak, peak_src = load_peaks()
     per_call_ms = np.median(res["per_call_ms"], axis=0)
     rows = []
@@ -364,10 +375,13 @@ def main():
         "vs_baseline": None, "dtype": "bf16" if dprob.kv_dtype == inputs.KV_BF16 else "bf16 (fp8 e4m3 cache)",
         "data": "synthetic",
         "config": {**desc, "parallelism": "replicas" if world > 1 else "single",
-                   "l2": ("flushed before every call (256 MB write)" if args.l2 == "flush" else
-                          "inputs larger than L2: each call of the step reads its own cache, "
-                          f"{sum(c['prob'].kv.numel() * c['prob'].kv.element_size() for c in res['calls']) / 1e6:.0f} MB in total > 126 MB L2"),
-                   "timing": "CUDA-graph replay, CUDA events per call, median over steps", "per_call": rows},
+                   "l2": ("flushed before every graph replay (256 MB write)" if args.l2 == "flush" else
+                          "inputs larger than L2: every call reads its own cache, "
+                          f"{args.graph_calls * sum(c['prob'].kv.numel() * c['prob'].kv.element_size() for c in res['calls']) / 1e6:.0f} MB in total > 126 MB L2"),
+                   "timing": (f"each call captured {args.graph_calls} times back to back in one CUDA graph (a cache "
+                              "of its own per copy); CUDA events around the replay; time per call = graph time / "
+                              f"{args.graph_calls}; a step replays every call's graph; median over steps"),
+                   "calls_per_step": calls_per_step * args.graph_calls, "per_call": rows},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4),
                      "traffic": (profiled_traffic(os.path.join(ROOT, "mla_speculative_verify_gb300", "csrc",
