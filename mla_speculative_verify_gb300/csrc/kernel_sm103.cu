@@ -880,11 +880,13 @@ constexpr int kMergeMaxSplits = 2048;
 template <int W>
 __global__ void __launch_bounds__(32 * W) lse_merge_kernel(const PlanMerge* merges, const float* part_o,
                                                                  const float* part_lse, __nv_bfloat16* out, float* lse) {
-  ptx::pdl_wait_primary();
   __shared__ float w_s[kMergeMaxSplits];
   __shared__ float red[W][2];
   __shared__ float4 acc_s[W][32];
+  // the merge item is plan data, written before the fold kernel ran: read it while the
+  // fold kernel finishes, then wait for the partials
   const PlanMerge m = merges[blockIdx.y];
+  ptx::pdl_wait_primary();
   const int row = blockIdx.x >> 2, quarter = blockIdx.x & 3;
   if (row >= m.nrows) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -978,8 +980,8 @@ __global__ void __launch_bounds__(32 * kMergeSmallWarps) lse_merge_small_kernel(
                                                                                 const float* part_o,
                                                                                 const float* part_lse,
                                                                                 __nv_bfloat16* out, float* lse) {
+  const PlanMerge m = merges[blockIdx.y];  // plan data: read before the wait, as above
   ptx::pdl_wait_primary();
-  const PlanMerge m = merges[blockIdx.y];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int idx = blockIdx.x * kMergeSmallWarps + warp;
   const int row = idx >> 2, quarter = idx & 3;
