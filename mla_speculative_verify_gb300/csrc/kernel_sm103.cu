@@ -432,13 +432,10 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
         }
       }
     }
-    if (softmax_any(need || fail)) {
-      if (softmax_any(fail || *abort != 0)) {
-        stop = true;
-        break;
-      }
-      // column maxima over this tile's keys (16 keys per half-warp), then move each
-      // row's reference up to its maximum
+    // Moving the references (rare once a row has seen its largest scores): column maxima
+    // over this tile's keys (16 keys per half-warp), each row's reference up to its maximum,
+    // l and O^T (tiles < t, once PV(t-1) is done) rescaled by alpha.
+    auto move_refs = [&]() {
 #pragma unroll
       for (int i = 0; i < NC; ++i) {
         float m = x[i];
@@ -458,8 +455,7 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
 #pragma unroll
       for (int i = 0; i < NC; ++i) l_acc[i] *= ms->alpha[16 * (i / 4) + col0 + (i % 4)];
       if (t >= 1) {
-        // O^T holds tiles < t: wait for PV(t-1), then scale each row's column by alpha
-        // (this warp: value blocks 2 grp and 2 grp + 1 of its lane quadrant)
+        // this warp: value blocks 2 grp and 2 grp + 1 of its lane quadrant
         fail = !warp_wait(&ms->pt_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, p.status);
         if (!fail) {
           ptx::tc_fence_after();
@@ -482,44 +478,41 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
           ptx::tmem_st_wait();
         }
       }
-    }
-    // probabilities relative to the (possibly moved) reference, packed to bf16, or for the
-    // e4m3 path times 2^4 and split into hi + lo e4m3 parts
+    };
+    // probabilities relative to the current references (pv, kept until l takes them),
+    // packed to bf16, or for the e4m3 path times 2^4 and split into hi + lo e4m3 parts
+    float pv[NC];
     uint32_t pk[NC / 2];
     uint32_t ph[NCH], pl[NCH];
-    if (!fail) {
+    auto make_p = [&]() {
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         const int n0 = 16 * c + col0;
         const float4 rr = *reinterpret_cast<const float4*>(&ms->ref[n0]);
         const float rrv[4] = {rr.x, rr.y, rr.z, rr.w};
-        float pv[4];
-        if (unmasked) {  // no masked score, and every row's reference is finite
+        if (unmasked) {  // no masked score (a reference may still be -inf: then a move follows)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) pv[j] = ex2(x[4 * c + j] - rrv[j]);
+          for (int j = 0; j < 4; ++j) pv[4 * c + j] = ex2(x[4 * c + j] - rrv[j]);
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const float v = x[4 * c + j];
-            pv[j] = v == -INFINITY ? 0.f : ex2(v - rrv[j]);
+            pv[4 * c + j] = v == -INFINITY ? 0.f : ex2(v - rrv[j]);
           }
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) l_acc[4 * c + j] += pv[j];
         if constexpr (kFp8) {
           uint32_t h01, l01, h23, l23;
-          split_e4m3x2(pv[0], pv[1], h01, l01);
-          split_e4m3x2(pv[2], pv[3], h23, l23);
+          split_e4m3x2(pv[4 * c], pv[4 * c + 1], h01, l01);
+          split_e4m3x2(pv[4 * c + 2], pv[4 * c + 3], h23, l23);
           ph[c] = h01 | (h23 << 16);
           pl[c] = l01 | (l23 << 16);
         } else {
-          pk[2 * c] = pack_bf16(pv[0], pv[1]);
-          pk[2 * c + 1] = pack_bf16(pv[2], pv[3]);
+          pk[2 * c] = pack_bf16(pv[4 * c], pv[4 * c + 1]);
+          pk[2 * c + 1] = pack_bf16(pv[4 * c + 2], pv[4 * c + 3]);
         }
       }
-      if (t >= 2) fail = !warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p.status);
-    }
-    if (!fail) {
+    };
+    auto store_p = [&]() {
       if constexpr (kFp8) {
         // e4m3 P^T hi and lo, MN-major with 64-byte rows (64-byte swizzle): key krow's row
         uint8_t* line_hi = a.sPt + sb * kPtBytes + krow * 64;
@@ -551,23 +544,58 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
       }
       ptx::fence_async_smem();
       ptx::tc_fence_before();
-    }
+    };
     if constexpr (kFp8) {
-      // the O^T warp issues O^T(t) once all softmax warps have arrived; a warp that gave
-      // up a wait leaves the loop with the others at the next tile's vote
+      // e4m3: the vote comes first, then P^T; the O^T warp issues O^T(t) once all softmax
+      // warps have arrived (a warp that gave up a wait leaves the loop with the others at
+      // the next tile's vote)
+      if (softmax_any(need || fail)) {
+        if (softmax_any(fail || *abort != 0)) {
+          stop = true;
+          break;
+        }
+        move_refs();
+      }
       if (!fail) {
+        make_p();
+        if (t >= 2) fail = !warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p.status);
+      }
+      if (!fail) {
+#pragma unroll
+        for (int i = 0; i < NC; ++i) l_acc[i] += pv[i];
+        store_p();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&ms->p_full[sb]);
       }
       continue;
     }
-    // P^T(t) is complete once every softmax warp is past this barrier (which also ends the
-    // loop in all warps together if one of them gave up a wait); then warps 0..3 each issue
+    // bf16: P^T(t) is written with the current references before the vote, so that in the
+    // usual tile (no reference moves) one barrier both votes and closes P^T(t); if a row
+    // must move, the references move and P^T(t) is written again. The barriers also end the
+    // loop in all warps together if one of them gave up a wait. Then warps 0..3 each issue
     // one value block of O^T(t) and release the page slot and the P^T buffer.
-    if (softmax_any(fail || *abort != 0)) {
-      stop = true;
-      break;
+    if (!fail) {
+      make_p();
+      if (t >= 2) fail = !warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p.status);
     }
+    if (!fail) store_p();
+    if (softmax_any(need || fail || *abort != 0)) {
+      if (softmax_any(fail || *abort != 0)) {
+        stop = true;
+        break;
+      }
+      move_refs();
+      if (!fail) {
+        make_p();
+        store_p();
+      }
+      if (softmax_any(fail || *abort != 0)) {
+        stop = true;
+        break;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NC; ++i) l_acc[i] += pv[i];
     if (w8 < 4) {
       ptx::tc_fence_after();
       if (lane == 0) {
