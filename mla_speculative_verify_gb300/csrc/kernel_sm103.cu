@@ -38,11 +38,13 @@
 //              rescaled in TMEM, only when a score exceeds it by a few octaves (the
 //              conditional rescale of flashinfer PR #5602); then the epilogue: O / l to
 //              bf16 out and LSE, or fp32 partials for the merge kernel. The eight warps
-//              agree on every decision through OR-reducing named barriers; for a bf16
-//              cache, after the barrier that closes P^T(t), four of them each issue one
-//              value block of O^T(t) += V^T P^T(t). (On the critical path of the two-stage
-//              bf16 page ring this saves a wake-up and issues the 16 MMAs four at a time;
-//              the e4m3 softmax is already the busiest role, so there a warp does it.)
+//              agree on every decision through OR-reducing named barriers. For a bf16
+//              cache P^T(t) is written with the current references first, so that one
+//              barrier per tile both votes on reference moves and closes P^T(t) (a move
+//              rewrites it); after it four of the warps each issue one value block of
+//              O^T(t) += V^T P^T(t). (On the critical path of the two-stage bf16 page ring
+//              this saves a wake-up and issues the 16 MMAs four at a time; the e4m3
+//              softmax is already the busiest role, so there a warp does it.)
 //
 // For an e4m3 cache the products run on kind::f8f6f4 MMAs straight from the cached
 // codes: each Q row is scaled by a power of two and split into two e4m3 parts (hi and
