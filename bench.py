@@ -351,24 +351,40 @@ def main():
     us_per_call = step_ms * 1000.0 / (calls_per_step * args.graph_calls)
     hbm_peak, tf_peak, peak_src = load_peaks()
     per_call_ms = np.median(res["per_call_ms"], axis=0)
+    def tensor_peak(prob):
+        # the contraction's own dtype: an e4m3 cache runs e4m3 MMAs, whose dense peak is the
+        # measured bf16 peak times the nominal 2x ratio
+        return tf_peak * (2.0 if prob.kv_dtype == inputs.KV_FP8 else 1.0)
+
     rows = []
     for c, ms in zip(res["calls"], per_call_ms):
         prob = c["prob"]
         nbytes = algorithmic_bytes(prob)
         flops = algorithmic_flops(prob)
         gbs = nbytes / (ms * 1e-3) / 1e9
+        hf, tf = gbs / hbm_peak, flops / (ms * 1e-3) / 1e12 / tensor_peak(prob)
         rows.append(dict(name=prob.name, us=round(ms * 1000.0, 2), kv_gbs=round(gbs, 1),
-                         hbm_frac=round(gbs / hbm_peak, 3),
-                         tensor_frac=round(flops / (ms * 1e-3) / 1e12 / tf_peak, 3),
+                         hbm_frac=round(hf, 3), tensor_frac=round(tf, 3), combined_frac=round(max(hf, tf), 3),
                          units=c["dec"].info["n_units"], merge_items=c["dec"].info["n_merge"]))
     # roofline of the dominant kernel (the fold kernel, launched once per call; each timed
-    # call is the whole mla_decode_run, fold + merge): the step's algorithmic bytes over the
-    # step's call time, i.e. per average launch, against the measured HBM copy peak
+    # call is the whole mla_decode_run, fold + merge): the step's algorithmic bytes (or
+    # flops, when the step's tensor time at peak exceeds its HBM time) over the step's call
+    # time, i.e. per average launch, against the measured peak
     dom = int(np.argmax(per_call_ms))
     dprob = res["calls"][dom]["prob"]
     n_calls = len(res["calls"])
     dbytes = sum(algorithmic_bytes(c["prob"]) for c in res["calls"]) // n_calls
-    achieved = dbytes / (float(per_call_ms.mean()) * 1e-3) / 1e9
+    dflops = sum(algorithmic_flops(c["prob"]) for c in res["calls"]) / n_calls
+    t_hbm = sum(algorithmic_bytes(c["prob"]) / (hbm_peak * 1e9) for c in res["calls"])
+    t_tensor = sum(algorithmic_flops(c["prob"]) / (tensor_peak(c["prob"]) * 1e12) for c in res["calls"])
+    tensor_bound = t_tensor > t_hbm
+    call_s = float(per_call_ms.mean()) * 1e-3
+    achieved = dflops / call_s / 1e12 if tensor_bound else dbytes / call_s / 1e9
+    # for a step that mixes bf16 and e4m3 calls, the peak that gives each call its own
+    # dtype's peak time (sum of flops over sum of flops / peak)
+    peak = round(n_calls * dflops / (t_tensor * 1e12), 1) if tensor_bound else hbm_peak
+    profile = {"sweep131k": "fold_decode_kernel_h12_q8_ctx131072_bf16.md",
+               "long_fp8": "fold_decode_kernel_h12_q8_ctx1048576_fp8.md"}.get(args.workload)
     line = {
         "metric": METRIC, "value": round(us_per_call, 3), "unit": "us/call", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": False, "scaling": "weak",
@@ -382,20 +398,21 @@ def main():
                               "of its own per copy); CUDA events around the replay; time per call = graph time / "
                               f"{args.graph_calls}; a step replays every call's graph; median over steps"),
                    "calls_per_step": calls_per_step * args.graph_calls, "per_call": rows},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4),
+        "roofline": {"bound": "tensor" if tensor_bound else "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "TFLOP/s" if tensor_bound else "GB/s",
+                     "frac": round(achieved / peak, 4),
                      "traffic": (profiled_traffic(os.path.join(ROOT, "mla_speculative_verify_gb300", "csrc",
                                                                "kernel_sm103.cu"),
-                                                  os.path.join(ROOT, "profiles",
-                                                               "fold_decode_kernel_h12_q8_ctx131072_bf16.md"))
-                                 if args.workload == "sweep131k" else None),
-                     "traffic_note": "ncu DRAM read+write bytes of one fold launch (the q=8 call; the "
+                                                  os.path.join(ROOT, "profiles", profile))
+                                 if profile else None),
+                     "traffic_note": "ncu DRAM read+write bytes of one fold launch (sweep: the q=8 call; the "
                                      "other calls read the same cache), from the committed profile when its "
                                      "kernel source hash matches, else null",
-                     "algorithmic_bytes": dbytes,
+                     "algorithmic_bytes": dbytes, "algorithmic_flops": dflops,
                      "kernel": "fold_decode_kernel + lse_merge_kernel, per mla_decode_run call, mean over "
                                f"the step's {n_calls} calls",
-                     "peak_source": f"{peak_src} hbm_gbs"},
+                     "peak_source": (f"{peak_src} bf16_tflops for bf16 calls, x 2 (nominal ratio) for e4m3 calls"
+                                     if tensor_bound else f"{peak_src} hbm_gbs")},
         "clocks": res["clocks"],
         "gpu_launches": res["launches"],
         "e2e": {"value": round(res["e2e"]["us_per_call"], 2), "unit": "us/call",
