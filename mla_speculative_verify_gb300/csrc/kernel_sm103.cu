@@ -27,7 +27,8 @@
 // Warp roles (one CTA per SM):
 //   warp 0     TMA producer: the Q tile once (bf16 cache), then one page per stage
 //              (two bf16 stages, or four e4m3 stages, in the same ring), each copy with
-//              an L2 prefetch of the page that enters the ring next
+//              an L2 prefetch of the page that enters the ring next (bf16: those of the
+//              first S copies leave once page 0 has landed)
 //   warps 1-2  S^T issue (one lane each) into buffer t % 2: bf16 partial p of every
 //              page, or every other page for e4m3
 //   warp 3     e4m3 only: O^T issue, the four value blocks of O^T += V^T P^T(t)
@@ -752,8 +753,9 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
       // page ids 32 at a time (one per lane), the next batch read one batch ahead. An id
       // outside the cache is reported and replaced by page 0. With the copy of page t the
       // producer also asks L2 for page t + S, the next one to enter the ring, so that its
-      // copy (issued once O^T(t) frees the slot) is served by L2. (Prefetching four pages
-      // beyond the ring measured slower: those requests queue in front of the ring's own.)
+      // copy (issued once O^T(t) frees the slot) is served by L2; for a bf16 cache the
+      // first S of these wait until page 0 has landed. (Prefetching four pages beyond the
+      // ring measured slower: those requests queue in front of the ring's own.)
       auto checked = [&](int pid, int t) {
         if (t < ntiles && (pid < 0 || pid >= p.num_pages)) {
           report(p.status, MLA_DEVICE_BAD_PAGE);
@@ -777,12 +779,24 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
             if (ok) {
               ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], G::kSlot);
               ptx::tma_load_3d(sKv + slot * G::kSlot, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0);
-              if (t0 + tp < ntiles) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, page_pf * kPage, 0);
+              if ((kFp8 || t >= S) && t0 + tp < ntiles) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, page_pf * kPage, 0);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           issued = t + 1;
+          if (!kFp8 && t == S - 1) {
+            // bf16: the prefetches that go with the first S copies leave once page 0 has
+            // landed, so that the first pages do not share HBM with them
+            int pf[S];
+#pragma unroll
+            for (int k = 0; k < S; ++k) pf[k] = __shfl_sync(0xffffffffu, pid_cur, S + k);
+            if (lane == 0 && wait_bar(&ms->kv_full[0], 0, abort, p.status)) {
+#pragma unroll
+              for (int k = 0; k < S; ++k)
+                if (S + k < ntiles) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, pf[k] * kPage, 0);
+            }
+          }
         }
         pid_cur = pid_next;
         pid_next = (t0 + 64 < ntiles) ? load_ids(t0 + 64) : 0;
