@@ -5,7 +5,8 @@ brute-force evaluation, a library routine, a closed form or an invariant:
   * brute force: numpy, the fully materialised masked score matrix;
   * library: torch float64 scaled_dot_product_attention (unmasked q=1, and an
     explicit bottom-right causal mask for q>1) and torch's float8_e4m3fn cast;
-  * closed forms: constant value rows, identical key rows;
+  * closed forms: constant value rows, identical key rows, and a hand-worked call
+    (tests/golden/closed_form_h1_q2_ctx3.json) through a permuted paged layout;
   * invariants: the causal rule, fold == direct, split + merge == direct, and
     the kv_scale homogeneity of an fp8 cache.
 """
@@ -214,3 +215,18 @@ def test_rejects_bad_arguments():
                          page_size=4)
     with pytest.raises(ValueError):
         run_oracle(bad)
+
+
+@pytest.mark.parametrize("mode", [oracle.MODE_DIRECT, oracle.MODE_FOLDED, oracle.MODE_SPLIT])
+def test_closed_form_golden_fixture(mode):
+    """The hand-worked call of tests/golden/closed_form_h1_q2_ctx3.json: pages of two keys
+    stored out of order, NaN in every cache row that holds no key of the request."""
+    from tests import golden_fixture
+    g = golden_fixture.load("closed_form_h1_q2_ctx3.json", page_size=2, page_order=[2, 0])
+    bounds = [[0, 1, 3]] if mode == oracle.MODE_SPLIT else None
+    out, lse = oracle.decode(g["q"].view(torch.int16).numpy().view(np.uint16),
+                             g["kv"].view(torch.int16).numpy().view(np.uint16), oracle.KV_BF16, 1.0,
+                             g["page_table"], 2, g["seq_lens"], g["q_lens"], g["H"], g["sm_scale"],
+                             mode=mode, split_bounds=bounds)
+    np.testing.assert_allclose(out, g["out"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, g["lse"], rtol=0, atol=1e-12)

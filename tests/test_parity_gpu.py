@@ -195,3 +195,20 @@ def test_full_size_h12_1m_sampled(kv):
     toks = [0, 7]
     o_ref, l_ref = oracle_rows(prob, toks)
     assert_close(out[toks], lse[toks], o_ref, l_ref)
+
+
+def test_closed_form_golden_fixture_gpu():
+    """The hand-worked call of tests/golden/closed_form_h1_q2_ctx3.json through the C ABI:
+    its page stored as physical page 1 of two, NaN in every other cache row."""
+    from mla_speculative_verify_gb300.decoder import VerifyDecoder
+    from tests import golden_fixture
+    g = golden_fixture.load("closed_form_h1_q2_ctx3.json", page_size=64, page_order=[1])
+    dec = VerifyDecoder(g["seq_lens"], g["q_lens"], g["H"], "bf16", "cuda")
+    out = torch.full((2, 1, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((2, 1), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dec.run(g["q"].cuda(), g["kv"].cuda(), torch.from_numpy(g["page_table"]).cuda(), out, lse,
+            g["sm_scale"], 1.0, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_close(out.float().cpu().numpy(), lse.cpu().numpy(), g["out"], g["lse"])
