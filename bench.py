@@ -6,7 +6,7 @@ ctx = 131072 with a bf16 paged cache (the q x ctx sweep of sglang PR #33650,
 per call in microseconds; the KV bandwidth and the roofline fraction go beside it.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                        [--workload sweep131k|long_bf16|long_fp8|h96|ragged48|ragged128]
+                        [--workload sweep131k|contig4096|long_bf16|long_fp8|h96|ragged48|ragged128]
 
 Timing: each call is captured R times back to back (--graph-calls, default 4) in one
 CUDA graph, every copy reading a cache of its own, and the graph replay is bracketed by
@@ -46,6 +46,9 @@ def workload(name: str):
     if name == "sweep131k":
         return [inputs.workload_sweep_131k(q) for q in (1, 2, 4, 8)], dict(
             workload="h12_ctx131072_bf16_q1-2-4-8", H=12, ctx=131072, q=[1, 2, 4, 8], kv="bf16", page_size=64)
+    if name == "contig4096":
+        return [inputs.workload_contiguous_small()], dict(workload="h12_q2_ctx4096_bf16_contiguous", H=12, ctx=4096,
+                                                         q=[2], kv="bf16", page_size=64)
     if name == "long_bf16":
         return [inputs.workload_long(inputs.KV_BF16)], dict(workload="h12_q8_ctx1048576_bf16", H=12, ctx=1 << 20, q=[8],
                                                              kv="bf16", page_size=64)

@@ -1,0 +1,49 @@
+"""Host-side pins of the benchmark's roofline arithmetic (CPU): the algorithmic bytes and
+flops of a call, worked out by hand for small batches, and the JSON line of the oracle
+(reference) arm on the smallest workload."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+import bench
+from mla_speculative_verify_gb300 import inputs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_algorithmic_bytes_and_flops_by_hand():
+    # two requests, H = 12: ctx 1000 (q = 4) and ctx 65 (q = 1), bf16 cache
+    prob = inputs.make_problem(12, [1000, 65], [4, 1], inputs.KV_BF16, seed=1)
+    kv = (1000 + 65) * 576 * 2
+    q = 5 * 12 * 576 * 2
+    out = 5 * 12 * 512 * 2
+    lse = 5 * 12 * 4
+    pages = (16 + 2) * 4          # ceil(1000 / 64) + ceil(65 / 64) page ids
+    assert bench.algorithmic_bytes(prob) == kv + q + out + lse + pages
+    # visible keys: tokens of the first request see 997, 998, 999, 1000; the second 65
+    assert bench.algorithmic_flops(prob) == (997 + 998 + 999 + 1000 + 65) * 12 * 2176.0
+
+
+def test_algorithmic_bytes_fp8_cache_counts_one_byte_per_element():
+    bf = inputs.make_problem(12, [640], [2], inputs.KV_BF16, seed=2)
+    f8 = inputs.make_problem(12, [640], [2], inputs.KV_FP8, seed=2)
+    assert bench.algorithmic_bytes(bf) - bench.algorithmic_bytes(f8) == 640 * 576
+
+
+@pytest.mark.timeout(600)
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` on the small contiguous workload prints one JSON line
+    with the contract's keys; the oracle is its timed arm."""
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "contig4096", "--steps", "1",
+                        "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "config",
+              "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["higher_is_better"] is False
+    assert line["warmup"] >= 3 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
