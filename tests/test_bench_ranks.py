@@ -34,7 +34,7 @@ def _rank_main(rank, world, port, out):
 
 @pytest.mark.timeout(300)
 def test_max_over_ranks_gloo_world2():
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.start_processes(_rank_main, args=(2, _free_port(), out), nprocs=2, join=True, start_method="spawn")
     assert dict(out) == {0: 2.5, 1: 2.5}
 
