@@ -160,8 +160,9 @@ class ClockSampler:
                     reasons.add(nm)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        med = statistics.median(sm)
+        return {"sm_mhz": med, "sm_max_mhz": max(smax), "reasons": sorted(reasons), "samples": len(sm),
+                "below_70pct_of_max": med < 0.7 * max(smax)}
 
 
 def run_ours(args, probs, desc, rank, world):

@@ -47,3 +47,19 @@ def test_reference_arm_json_line():
     assert line["impl"] == "reference" and line["higher_is_better"] is False
     assert line["warmup"] >= 3 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_clock_summary_reads_reasons_and_flags_low_clocks(tmp_path):
+    """The nvidia-smi CSV of the timed region: median SM clock, the throttle reasons seen,
+    and the flag for a median below 0.7 of the maximum clock."""
+    c = bench.ClockSampler(0)
+    c.proc = object()  # as if sampling had run
+    c.path = str(tmp_path / "clocks.csv")
+    rows = ["0, 1200, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Active",
+            "0, 1300, 2070, 950.0, 0x0, Not Active, Active, Not Active, Not Active",
+            "0, 1250, 2070, 940.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    (tmp_path / "clocks.csv").write_text("index, clocks.sm\n" + "\n".join(rows) + "\n")
+    s = c.summary()
+    assert s["sm_mhz"] == 1250 and s["sm_max_mhz"] == 2070 and s["samples"] == 3
+    assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert s["below_70pct_of_max"] is True
