@@ -1,12 +1,14 @@
 """Benchmark of the MLA speculative-verify decode on GB300.
 
-One step = one verify-decode call for each q in {1, 2, 4, 8} at H = 12 and
-ctx = 131072 with a bf16 paged cache (the q x ctx sweep of sglang PR #33650,
-"Raw q x ctx sweep" table, at its 131k column). `value` is the mean device time
-per call in microseconds; the KV bandwidth and the roofline fraction go beside it.
+One step (default workload `sweep`) = one verify-decode call for each point of the
+q x ctx sweep of sglang PR #33650 ("Raw q x ctx sweep" table) that fits the task's
+configurations: H = 12, q in {1, 2, 4, 8} at ctx = 131072 with a bf16 paged cache, and
+q = 8 at ctx = 1,048,576 with a bf16 cache and with an fp8 e4m3 cache. `value` is the
+mean device time per call in microseconds over the step's calls; each call's KV
+bandwidth and roofline fractions go beside it in `per_call`.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                        [--workload sweep131k|contig4096|long_bf16|long_fp8|h96|ragged48|ragged128]
+                        [--workload sweep|sweep131k|contig4096|long_bf16|long_fp8|h96|ragged48|ragged128|prefill]
 
 Timing: each call is captured R times back to back (--graph-calls, default 4) in one
 CUDA graph, every copy reading a cache of its own, and the graph replay is bracketed by
@@ -39,10 +41,19 @@ from mla_speculative_verify_gb300 import inputs  # noqa: E402
 
 METRIC = "MLA verify-decode µs/call and KV GB/s as % of GB300 HBM peak, q×ctx sweep"
 L2_FLUSH_BYTES = 256 << 20
+# GB300 HBM3e bandwidth as rated by the vendor (nominal; the measured copy peak of
+# MEASURED_PEAKS.json is the roofline denominator, this one is reported beside it)
+HBM_RATED_GBS = 7900.0
+CSRC = os.path.join(ROOT, "mla_speculative_verify_gb300", "csrc")
 
 
 def workload(name: str):
     """List of problems making up one step, and a description."""
+    if name == "sweep":
+        probs = [inputs.workload_sweep_131k(q) for q in (1, 2, 4, 8)]
+        probs += [inputs.workload_long(inputs.KV_BF16), inputs.workload_long(inputs.KV_FP8)]
+        return probs, dict(workload="h12_sweep_q1-2-4-8_ctx131072_bf16+q8_ctx1048576_bf16+fp8", H=12,
+                           ctx=[131072, 1 << 20], q=[1, 2, 4, 8], kv=["bf16", "fp8_e4m3"], page_size=64)
     if name == "sweep131k":
         return [inputs.workload_sweep_131k(q) for q in (1, 2, 4, 8)], dict(
             workload="h12_ctx131072_bf16_q1-2-4-8", H=12, ctx=131072, q=[1, 2, 4, 8], kv="bf16", page_size=64)
@@ -82,22 +93,39 @@ def algorithmic_flops(prob) -> float:
     return f
 
 
-def profiled_traffic(kernel_src: str, profile_md: str):
-    """DRAM bytes per launch from a committed ncu summary, or None when the kernel source
-    changed since the counters were taken (the summary records the source hash)."""
+def kernel_source_hash() -> str:
+    """sha256[:16] over the library's CUDA sources (sorted), recorded in each ncu summary."""
     import hashlib
+
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(CSRC, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile_md: str) -> dict:
+    """DRAM read + write bytes of one fold-kernel launch per call name, from a committed
+    ncu summary (lines `traffic[<call>]: <bytes>`); empty when the summary is missing or
+    the kernel sources changed since its counters were taken (it records their hash)."""
     import re
 
     try:
         text = open(profile_md).read()
-        sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
     except OSError:
-        return None
+        return {}
     m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    m_tr = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
-    if not m_sha or not m_tr or m_sha.group(1) != sha:
-        return None
-    return int(m_tr.group(1))
+    if not m_sha or m_sha.group(1) != kernel_source_hash():
+        return {}
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"traffic\[([\w.+-]+)\]:\s*(\d+)", text)}
+
+
+def mma_dtype(prob) -> str:
+    """Arithmetic type of a call's tensor-core products: bf16 x bf16 for a bf16 cache; for
+    an e4m3 cache e4m3 x e4m3 on the stored codes and on two-part (hi + lo) e4m3 operands
+    of Q and P; fp32 accumulation and softmax either way."""
+    return "bf16" if prob.kv_dtype == inputs.KV_BF16 else "e4m3 (hi+lo operands)"
 
 
 def load_peaks():
@@ -116,21 +144,30 @@ class ClockSampler:
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
+        import tempfile
+
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        fd, self.path = tempfile.mkstemp(prefix=f"mla_bench_clocks_gpu{gpu_index}_", suffix=".csv")
+        os.close(fd)
 
     def __enter__(self):
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                                          "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
+
+    def mark(self):
+        """Remember where the samples of the timed region begin (the file's current size)."""
+        try:
+            self.start = os.path.getsize(self.path)
+        except OSError:
+            self.start = 0
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -146,7 +183,17 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        with open(self.path) as fh:
+            text = fh.read()
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        lines = text.splitlines()
+        timed = text[getattr(self, "start", 0):].splitlines()
+        if sum(1 for ln in timed if len(ln.split(",")) >= 9) > 0:
+            lines = timed  # samples taken during the timed region only, when there are any
+        for line in lines:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -216,6 +263,7 @@ def run_ours(args, probs, desc, rank, world):
     torch.cuda.synchronize(dev)
     all_evs = []
     with ClockSampler(dev.index) as clk:
+        clk.mark()
         t0 = time.perf_counter()
         for _ in range(args.steps):
             all_evs.append(one_step(True))
@@ -279,27 +327,52 @@ def measure_e2e(args, calls, dev, stream):
     return dict(ms_per_step=ms, us_per_call=ms * 1000.0 / len(calls), h2d=h2d, d2h=d2h)
 
 
-def cpu_baseline(probs, max_seconds=30.0):
-    """The float64 oracle, as it stands, on this host's cores: one call per problem of
-    the step (time-bounded: stop after max_seconds and scale by the calls done)."""
+def visible_key_rows(seq_lens, q_lens, H) -> int:
+    """Sum over the query rows of the keys each one sees (the causal rule): the oracle's
+    work is proportional to it."""
+    n = 0
+    for ctx, q in zip(seq_lens, q_lens):
+        n += sum(int(ctx) - int(q) + i + 1 for i in range(int(q))) * H
+    return n
+
+
+def oracle_sample(prob, tokens: int = 2):
+    """A bounded sample of one call for the float64 oracle: the first `tokens` verify
+    tokens of the first request, at its full context (token i keeps its causal key
+    range), and the factor that scales the sample's time to the whole call (visible
+    key-rows of the call over those of the sample)."""
+    ctx, q = int(prob.seq_lens[0]), int(prob.q_lens[0])
+    t = max(1, min(q, tokens))
+    sub = inputs.Problem(H=prob.H, seq_lens=np.array([ctx - q + t], np.int32), q_lens=np.array([t], np.int32),
+                         page_table=prob.page_table[:1], q=prob.q[:t].clone(), kv=prob.kv, kv_dtype=prob.kv_dtype,
+                         kv_scale=prob.kv_scale, sm_scale=prob.sm_scale)
+    scale = visible_key_rows(prob.seq_lens, prob.q_lens, prob.H) / visible_key_rows(sub.seq_lens, sub.q_lens, prob.H)
+    return sub, scale
+
+
+def cpu_baseline(probs, tokens: int = 2):
+    """The float64 oracle, as it stands (split + merge mode, 64 key chunks per request),
+    on this host's cores, over a bounded sample of every call of the step: the first
+    `tokens` verify tokens of each call at full context, timed and scaled to the whole
+    call by its visible key-rows."""
     import oracle
 
     oracle.build()
     cores = os.cpu_count() or 1
-    t_total, done = 0.0, 0
+    us = []
     for prob in probs:
-        kvd = oracle.KV_BF16 if prob.kv_dtype == inputs.KV_BF16 else oracle.KV_FP8_E4M3
-        bounds = [sorted(set(int(c) * i // 64 for i in range(65))) for c in prob.seq_lens]
+        sub, scale = oracle_sample(prob, tokens)
+        kvd = oracle.KV_BF16 if sub.kv_dtype == inputs.KV_BF16 else oracle.KV_FP8_E4M3
+        bounds = [sorted(set(int(c) * i // 64 for i in range(65))) for c in sub.seq_lens]
         t0 = time.perf_counter()
-        oracle.decode(prob.q_bits(), prob.kv_bits(), kvd, prob.kv_scale, prob.page_table, prob.page_size,
-                      prob.seq_lens, prob.q_lens, prob.H, prob.sm_scale, mode=oracle.MODE_SPLIT, split_bounds=bounds,
+        oracle.decode(sub.q_bits(), sub.kv_bits(), kvd, sub.kv_scale, sub.page_table, sub.page_size,
+                      sub.seq_lens, sub.q_lens, sub.H, sub.sm_scale, mode=oracle.MODE_SPLIT, split_bounds=bounds,
                       nthreads=cores)
-        t_total += time.perf_counter() - t0
-        done += 1
-        if t_total > max_seconds:
-            break
-    return dict(us_per_call=t_total * 1e6 / done, cores=cores, calls=done,
-                sample=f"{done} of {len(probs)} calls of the step, full size, oracle split+merge mode")
+        us.append((time.perf_counter() - t0) * 1e6 * scale)
+    return dict(us_per_call=float(np.mean(us)), cores=cores, calls=len(probs),
+                sample=(f"every call of the step ({len(probs)}), each on its first {tokens} verify tokens of the "
+                        "first request at full context, oracle split+merge mode; time scaled to the whole call by "
+                        "visible key-rows"))
 
 
 def max_over_ranks(x: float, device) -> float:
@@ -319,7 +392,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="sweep131k")
+    ap.add_argument("--workload", default="sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph-calls", type=int, default=4, choices=range(1, 65), metavar="1..64",
                     help="copies of each call, each on a cache of its own, captured back to back in the call's "
@@ -345,7 +418,7 @@ def main():
             return
         times = []
         for i in range(args.warmup + args.steps):
-            r = cpu_baseline(probs, max_seconds=20.0)
+            r = cpu_baseline(probs)
             if i >= args.warmup:
                 times.append(r["us_per_call"])
         v = statistics.median(times)
@@ -370,6 +443,7 @@ def main():
         # measured bf16 peak times the nominal 2x ratio
         return tf_peak * (2.0 if prob.kv_dtype == inputs.KV_FP8 else 1.0)
 
+    traffic = profiled_traffic(os.path.join(ROOT, "profiles", f"dram_traffic_{args.workload}.md"))
     rows = []
     for c, ms in zip(res["calls"], per_call_ms):
         prob = c["prob"]
@@ -377,15 +451,15 @@ def main():
         flops = algorithmic_flops(prob)
         gbs = nbytes / (ms * 1e-3) / 1e9
         hf, tf = gbs / hbm_peak, flops / (ms * 1e-3) / 1e12 / tensor_peak(prob)
-        rows.append(dict(name=prob.name, us=round(ms * 1000.0, 2), kv_gbs=round(gbs, 1),
-                         hbm_frac=round(hf, 3), tensor_frac=round(tf, 3), combined_frac=round(max(hf, tf), 3),
-                         units=c["dec"].info["n_units"], merge_items=c["dec"].info["n_merge"]))
+        rows.append(dict(name=prob.name, dtype=mma_dtype(prob), us=round(ms * 1000.0, 2), kv_gbs=round(gbs, 1),
+                         hbm_frac=round(hf, 3), hbm_frac_rated=round(gbs / HBM_RATED_GBS, 3),
+                         tensor_frac=round(tf, 3), combined_frac=round(max(hf, tf), 3),
+                         traffic=traffic.get(prob.name), units=c["dec"].info["n_units"],
+                         merge_items=c["dec"].info["n_merge"]))
     # roofline of the dominant kernel (the fold kernel, launched once per call; each timed
     # call is the whole mla_decode_run, fold + merge): the step's algorithmic bytes (or
     # flops, when the step's tensor time at peak exceeds its HBM time) over the step's call
     # time, i.e. per average launch, against the measured peak
-    dom = int(np.argmax(per_call_ms))
-    dprob = res["calls"][dom]["prob"]
     n_calls = len(res["calls"])
     dbytes = sum(algorithmic_bytes(c["prob"]) for c in res["calls"]) // n_calls
     dflops = sum(algorithmic_flops(c["prob"]) for c in res["calls"]) / n_calls
@@ -397,15 +471,16 @@ def main():
     # for a step that mixes bf16 and e4m3 calls, the peak that gives each call its own
     # dtype's peak time (sum of flops over sum of flops / peak)
     peak = round(n_calls * dflops / (t_tensor * 1e12), 1) if tensor_bound else hbm_peak
-    profile = {"sweep131k": "fold_decode_kernel_h12_q8_ctx131072_bf16.md",
-               "long_fp8": "fold_decode_kernel_h12_q8_ctx1048576_fp8.md"}.get(args.workload)
+    call_traffic = [traffic.get(c["prob"].name) for c in res["calls"]]
+    mean_traffic = int(sum(call_traffic) / n_calls) if all(t is not None for t in call_traffic) else None
+    dtypes = sorted({mma_dtype(c["prob"]) for c in res["calls"]})
     line = {
         "metric": METRIC, "value": round(us_per_call, 3), "unit": "us/call", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if dprob.kv_dtype == inputs.KV_BF16 else "bf16 (fp8 e4m3 cache)",
-        "data": "synthetic",
+        "vs_baseline": None, "dtype": " + ".join(dtypes), "data": "synthetic",
         "config": {**desc, "parallelism": "replicas" if world > 1 else "single",
                    "value_note": "whole job: the slowest rank's step time over the calls all ranks ran",
+                   "dtype_note": "per call: the tensor-core operand type (fp32 accumulation and softmax)",
                    "l2": ("flushed before every graph replay (256 MB write)" if args.l2 == "flush" else
                           "inputs larger than L2: every call reads its own cache, "
                           f"{args.graph_calls * sum(c['prob'].kv.numel() * c['prob'].kv.element_size() for c in res['calls']) / 1e6:.0f} MB in total > 126 MB L2"),
@@ -416,18 +491,18 @@ def main():
         "roofline": {"bound": "tensor" if tensor_bound else "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "TFLOP/s" if tensor_bound else "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": (profiled_traffic(os.path.join(ROOT, "mla_speculative_verify_gb300", "csrc",
-                                                               "kernel_sm103.cu"),
-                                                  os.path.join(ROOT, "profiles", profile))
-                                 if profile else None),
-                     "traffic_note": "ncu DRAM read+write bytes of one fold launch (sweep: the q=8 call; the "
-                                     "other calls read the same cache), from the committed profile when its "
-                                     "kernel source hash matches, else null",
+                     "traffic": mean_traffic,
+                     "traffic_note": ("ncu DRAM read+write bytes of one fold launch, mean over the step's calls, "
+                                      "from the committed profile when the hash of the kernel sources matches, "
+                                      "else null"),
                      "algorithmic_bytes": dbytes, "algorithmic_flops": dflops,
                      "kernel": "fold_decode_kernel + lse_merge_kernel, per mla_decode_run call, mean over "
                                f"the step's {n_calls} calls",
                      "peak_source": (f"{peak_src} bf16_tflops for bf16 calls, x 2 (nominal ratio) for e4m3 calls"
-                                     if tensor_bound else f"{peak_src} hbm_gbs")},
+                                     if tensor_bound else f"{peak_src} hbm_gbs"),
+                     **({} if tensor_bound else {"peak_rated": HBM_RATED_GBS,
+                                                 "frac_rated": round(achieved / HBM_RATED_GBS, 4),
+                                                 "peak_rated_source": "GB300 HBM3e nominal 7.9 TB/s"})},
         "clocks": res["clocks"],
         "gpu_launches": res["launches"],
         "e2e": {"value": round(max_over_ranks(res["e2e"]["us_per_call"], "cuda") / world, 2), "unit": "us/call",

@@ -163,8 +163,9 @@ int mla_decode_run(const void* plan_dev, const void* plan_host, size_t plan_byte
  *   A plan whose workspace exceeds the array (mla_decode_plan reports the size) is
  *   rejected with MLA_ERR_BUFFER before any launch; plan with fewer splits
  *   (mla_plan_options.force_splits) or use mla_decode_run with your own workspace.
- *   The first call on a device looks up the array's device address (once, with that
- *   device current); make that first call before any stream capture.
+ *   The first call on a device looks up the array's device address (with that device
+ *   current) and caches it with the current context; make that first call before any
+ *   stream capture. After a device reset the next call looks it up again.
  *   Every call in the process shares the one array per device and overwrites what the
  *   previous call left in it; nothing in it needs clearing. Calls whose kernels
  *   overlap on the GPU (for example on two concurrent streams) race on the array, so

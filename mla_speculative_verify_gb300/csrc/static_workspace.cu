@@ -5,7 +5,10 @@
 // The array is a file-scope __device__ variable: every GPU that loads this library
 // holds MLA_STATIC_WORKSPACE_BYTES of it until the process exits. In host code the
 // variable's name is only a host-side stand-in, so its device address is fetched with
-// cudaGetSymbolAddress, once per device, with that device current, and cached.
+// cudaGetSymbolAddress, once per device and context, with that device current, and
+// cached together with the context it belongs to: after a device reset (a new primary
+// context) the next call looks the address up again instead of using a stale one.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -26,23 +29,46 @@ static __device__ __align__(256) unsigned char g_static_workspace[MLA_STATIC_WOR
 
 constexpr int kMaxDevices = 64;
 static void* g_static_ws_ptr[kMaxDevices];
+static CUcontext g_static_ws_ctx[kMaxDevices];
 static bool g_static_ws_ready[kMaxDevices];
 static std::mutex g_static_ws_mu;
 
-// Device address of the array on the current device (looked up on first use).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The calling thread's current context (the device's primary context once the runtime
+// has initialised it), or nullptr when the driver entry point is unavailable.
+static CUcontext current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (CtxGetCurrentFn)f;
+  });
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
+// Device address of the array on the current device (looked up on first use, and again
+// whenever the current context is not the one the cached address was taken in).
 static int static_workspace_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return set_error(MLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return set_error(MLA_ERR_CUDA, "device ordinal %d out of range", dev);
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lk(g_static_ws_mu);
-  if (!g_static_ws_ready[dev]) {
+  if (!g_static_ws_ready[dev] || g_static_ws_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_static_workspace);
     if (e != cudaSuccess || p == nullptr)
       return set_error(MLA_ERR_CUDA, "cudaGetSymbolAddress of the static workspace failed on device %d: %s", dev,
                        cudaGetErrorString(e));
     g_static_ws_ptr[dev] = p;
+    g_static_ws_ctx[dev] = current_context();  // the runtime call above made the context current
     g_static_ws_ready[dev] = true;
   }
   *out = g_static_ws_ptr[dev];

@@ -73,3 +73,22 @@ def oracle_rows(prob, tokens):
         outs.append(o[0])
         lses.append(l[0])
     return np.stack(outs), np.stack(lses)
+
+
+def sub_problem(prob, b: int, tokens=None):
+    """Request b of a batch as a problem of its own (its Q rows, seq_len, page-table row;
+    the cache is shared), optionally cut to its first `tokens` verify tokens with each
+    token's causal key range kept (token i of a request with ctx keys and q tokens sees
+    ctx - q + i + 1 keys)."""
+    ctx, q = int(prob.seq_lens[b]), int(prob.q_lens[b])
+    t = q if tokens is None else max(1, min(q, int(tokens)))
+    tok0 = int(prob.q_lens[:b].sum())
+    return inputs.Problem(H=prob.H, seq_lens=np.array([ctx - q + t], np.int32), q_lens=np.array([t], np.int32),
+                          page_table=prob.page_table[b:b + 1], q=prob.q[tok0:tok0 + t].clone(), kv=prob.kv,
+                          kv_dtype=prob.kv_dtype, kv_scale=prob.kv_scale, sm_scale=prob.sm_scale)
+
+
+def token_rows(prob, b: int) -> slice:
+    """Global token indices of request b (rows of out / lse)."""
+    tok0 = int(prob.q_lens[:b].sum())
+    return slice(tok0, tok0 + int(prob.q_lens[b]))

@@ -7,7 +7,7 @@ import torch
 
 from mla_speculative_verify_gb300 import inputs
 from mla_speculative_verify_gb300.binding import PlanOptions
-from tests.gpu_util import assert_close, oracle_rows, run_gpu, run_oracle, to_device
+from tests.gpu_util import assert_close, oracle_rows, run_gpu, run_oracle, sub_problem, to_device, token_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -212,3 +212,52 @@ def test_closed_form_golden_fixture_gpu():
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert_close(out.float().cpu().numpy(), lse.cpu().numpy(), g["out"], g["lse"])
+
+
+@pytest.mark.parametrize("q,ctx,kv", [(8, 131072, BF16), (8, 131072, FP8), (1, 131072, BF16), (1, 32768, FP8)])
+def test_full_size_h96_sampled(q, ctx, kv):
+    """H = 96 (fold F = 1: every token is a group of its own) at the full context, in
+    the plan the library makes for it; the first and last verify tokens against the
+    oracle."""
+    prob = inputs.workload_h96(q, ctx, kv)
+    out, lse, _ = run_gpu(prob)
+    toks = sorted({0, q - 1})
+    o_ref, l_ref = oracle_rows(prob, toks)
+    assert_close(out[toks], lse[toks], o_ref, l_ref)
+
+
+@pytest.mark.parametrize("H", [48, 128])
+@pytest.mark.parametrize("pattern", ["ragged", "uniform"])
+def test_full_size_ragged_batch_sampled(H, pattern):
+    """The B = 32 fp8 batches at their full contexts (16k-32k keys per request), in the
+    plan the library makes for the whole batch (its piece lengths and merge layout);
+    three requests (first, middle, last) against the oracle, each on its own."""
+    prob = inputs.workload_ragged(H, pattern)
+    out, lse, _ = run_gpu(prob)
+    for b in (0, prob.batch // 2, prob.batch - 1):
+        o_ref, l_ref = run_oracle(sub_problem(prob, b))
+        rows = token_rows(prob, b)
+        assert_close(out[rows], lse[rows], o_ref, l_ref)
+
+
+def test_bad_page_id_is_reported_not_faulted():
+    """A page id outside [0, num_pages) (one too large, one negative) in one request's
+    page table: the kernel reports MLA_DEVICE_BAD_PAGE, reads page 0 in its place (in
+    bounds), and the other request's output still matches the oracle."""
+    from mla_speculative_verify_gb300.binding import MLA_DEVICE_BAD_PAGE
+
+    prob = inputs.make_problem(12, [700, 900], [2, 4], BF16, seed=2950)
+    prob.page_table = prob.page_table.copy()
+    prob.page_table[0, 3] = prob.num_pages + 5
+    prob.page_table[0, 7] = -1
+    out, lse, st = run_gpu(prob, check_status=False)
+    assert st & MLA_DEVICE_BAD_PAGE
+    o_ref, l_ref = run_oracle(sub_problem(prob, 1))
+    rows = token_rows(prob, 1)
+    assert_close(out[rows], lse[rows], o_ref, l_ref)
+    # the context stays usable
+    good = inputs.make_problem(12, [700], [2], BF16, seed=2951)
+    o2, l2, st2 = run_gpu(good)
+    assert st2 == 0
+    o_ref2, l_ref2 = run_oracle(good)
+    assert_close(o2, l2, o_ref2, l_ref2)

@@ -4,16 +4,18 @@ an allocation synchronise the device, fixed memory plans). It takes its split-KV
 from a device array the library owns. This file is collected last on purpose: a failure
 here leaves every other GPU test already run.
 
-Checked through the C entry point against mla_decode_run with a caller workspace, on two
-calls in a row (the array keeps the previous call's contents), within the tolerance of
-the parity tests, plus the rejection of a plan whose scratch exceeds the array."""
+Checked through the C entry point against mla_decode_run with a caller workspace and
+against the float64 oracle, on two calls in a row (the array keeps the previous call's
+contents), within the tolerance of the parity tests; the device's free memory is the same
+before and after the second call (the entry point allocates nothing); and a plan whose
+scratch exceeds the array is rejected."""
 import pytest
 import torch
 
 from mla_speculative_verify_gb300 import binding, inputs
 from mla_speculative_verify_gb300.binding import PlanOptions
 from mla_speculative_verify_gb300.decoder import VerifyDecoder
-from tests.gpu_util import LSE_ATOL, OUT_ATOL, OUT_RTOL
+from tests.gpu_util import LSE_ATOL, OUT_ATOL, OUT_RTOL, assert_close, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -37,17 +39,23 @@ def test_static_workspace_matches_caller_workspace(kv_dtype, seq, qlen, H):
     ref_lse = torch.empty(shape, dtype=torch.float32, device="cuda")
     dec.run(q, kv, pt, ref_out, ref_lse, prob.sm_scale, prob.kv_scale)
     torch.cuda.synchronize()
-    for _ in range(2):
+    o_ref, l_ref = run_oracle(prob)
+    for call in range(2):
         out = torch.full(shape + (512,), float("nan"), dtype=torch.bfloat16, device="cuda")
         lse = torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         _call_static(dec, prob, q, kv, pt, out, lse, status)
         torch.cuda.synchronize()
+        if call == 1:  # the first call may still load the library's module on this device
+            assert torch.cuda.mem_get_info()[0] == free_before, "the static-workspace call allocated device memory"
         assert int(status.item()) == 0
         o, r = out.float(), ref_out.float()
         assert torch.isfinite(o).all()
         assert ((o - r).abs() <= OUT_ATOL + OUT_RTOL * r.abs()).all()
         assert (lse - ref_lse).abs().max().item() <= LSE_ATOL
+        assert_close(o.cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref)
 
 
 def test_static_workspace_rejects_a_plan_larger_than_the_array():
