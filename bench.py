@@ -69,6 +69,11 @@ def workload(name: str):
     if name == "h96":
         probs = [inputs.workload_h96(q, c, kv) for q in (1, 8) for c in (32768, 131072) for kv in ("bf16", "fp8")]
         return probs, dict(workload="h96_q1-8_ctx32768-131072_bf16-fp8", H=96, page_size=64)
+    if name == "prefill":
+        probs = [inputs.make_problem(H, [131072], [2048], inputs.KV_BF16, seed=1006, name=f"h{H}_q2048_ctx131072_bf16")
+                 for H in (12, 96)]
+        return probs, dict(workload="prefill_h12+h96_q2048_ctx131072_bf16", H=[12, 96], q=2048, ctx=131072,
+                           page_size=64)
     if name.startswith("ragged"):
         H = int(name[len("ragged"):])
         return [inputs.workload_ragged(H, "ragged"), inputs.workload_ragged(H, "uniform")], dict(

@@ -79,6 +79,11 @@ typedef struct {
   int min_pages_per_split; /* > 0: lower bound on pages per split unit */
   int force_fold;          /* > 0: use this fold factor F instead of the largest divisor rule
                               (must divide every q_len; F = 1 is the fold-less diagnostic mode) */
+  int debug_skip_copy;     /* test of the device timeout path only, 0 in production: > 0 makes
+                              the first work unit skip the copy of its page number
+                              debug_skip_copy - 1 and shortens every bounded wait of the call to
+                              ~2 ms, so the units that wait for that page report
+                              MLA_DEVICE_WAIT_TIMEOUT and stop (no fault, no hang) */
 } mla_plan_options;
 
 /*

@@ -16,36 +16,38 @@
 // MN-major (the latent cache rows hold V in columns 0..511; flashinfer PR #5602 "What
 // r52 changes": the latent K stages are held until PV).
 //
-// One thread issues a tcgen05.mma only every ~60 cycles, while an N = 16..48 MMA
-// needs 20..45 cycles of tensor time, so for a bf16 cache S^T is issued by two warps into
-// two partial accumulators (summed by the softmax), and O^T by four softmax warps (one value
-// block each) as soon as P^T is complete. For an e4m3 cache S^T takes half the MMAs
-// (K = 32) and multiplies each K step by Q_hi and Q_lo at once (N = 2 nmma), so the two S^T
-// warps take alternate pages, and a separate warp issues O^T. S^T is double-buffered in
-// tensor memory, so the product of the next page runs while the softmax works on this one.
+// One thread issues a tcgen05.mma only every ~100 cycles (~120 for the MN-major and e4m3
+// forms), whatever the MMA's N, while an N = 16..96 MMA needs 8..48 cycles of tensor time,
+// so the products of a page are issued from several threads: three MMA warps split the
+// K-steps of S^T into one accumulator (the first K-step, which overwrites it, comes from
+// the leader before the others start), and O^T, zeroed in tensor memory at the start of
+// the unit so that every O^T MMA accumulates, is issued by four softmax warps (one value
+// block each) for a bf16 cache, or shared by the three MMA warps for an e4m3 cache. For an
+// e4m3 cache each S^T K-step multiplies the page by Q_hi and Q_lo at once (N = 2 nmma).
+// S^T is double-buffered in tensor memory, so the product of the next page runs while the
+// softmax works on this one.
 //
 // Warp roles (one CTA per SM):
 //   warp 0     TMA producer: the Q tile once (bf16 cache), then one page per stage
 //              (two bf16 stages, or four e4m3 stages, in the same ring), each copy with
 //              an L2 prefetch of the page that enters the ring next (bf16: those of the
 //              first S copies leave once page 0 has landed)
-//   warps 1-2  S^T issue (one lane each) into buffer t % 2: bf16 partial p of every
-//              page, or every other page for e4m3
-//   warp 3     e4m3 only: O^T issue, the four value blocks of O^T += V^T P^T(t)
-//   8 softmax warps (3-10 for bf16, 4-11 for e4m3): each thread owns one key of the
-//              S^T tile (a TMEM lane) and a quarter of the columns of each 16-column
-//              chunk; online
+//   warps 1-3  MMA warps: a third of the K-steps of S^T(t) each, into buffer t % 2; for an
+//              e4m3 cache also a third of the MMAs of O^T(t - 1) += V^T P^T(t - 1). Warp 1
+//              leads: it does the waits, and the three vote on a named barrier
+//   warps 4-11 softmax: each thread owns one key of the S^T tile (a TMEM lane) and a
+//              quarter of the columns of each 16-column chunk; online
 //              softmax with a lazy per-row reference: the reference moves, and O^T is
 //              rescaled in TMEM, only when a score exceeds it by a few octaves (the
 //              conditional rescale of flashinfer PR #5602); then the epilogue: O / l to
-//              bf16 out and LSE, or fp32 partials for the merge kernel. The eight warps
+//              bf16 out and LSE, or bf16 partials for the merge kernel. The eight warps
 //              agree on every decision through OR-reducing named barriers. For a bf16
 //              cache P^T(t) is written with the current references first, so that one
 //              barrier per tile both votes on reference moves and closes P^T(t) (a move
 //              rewrites it); after it four of the warps each issue one value block of
 //              O^T(t) += V^T P^T(t). (On the critical path of the two-stage bf16 page ring
-//              this saves a wake-up and issues the 16 MMAs four at a time; the e4m3
-//              softmax is already the busiest role, so there a warp does it.)
+//              this saves a wake-up; the e4m3 softmax is already the busiest role, so there
+//              the MMA warps do it.)
 //
 // For an e4m3 cache the products run on kind::f8f6f4 MMAs straight from the cached
 // codes: each Q row is scaled by a power of two and split into two e4m3 parts (hi and
@@ -109,17 +111,27 @@ struct Geo {
 
 constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, each owning half of the columns
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
-// Warps: producer, MMA issuers, softmax. bf16: two S^T issuers, and O^T is issued by four
-// of the softmax warps (it is on the critical path of the two-stage page ring). e4m3: two
-// S^T issuers and an O^T warp (the softmax warps are the busiest there).
+// Warps: producer, MMA warps, softmax. Every accumulator is written by one thread in
+// program order, so a unit's result is the same bit for bit on every run.
+//   bf16:  three S^T warps, each a third of the K-steps into a partial accumulator of its
+//          own (the softmax adds the three); O^T is issued by four of the softmax warps,
+//          one value block each (it is on the critical path of the two-stage page ring)
+//   e4m3:  two S^T warps that take alternate pages (all K-steps of a page each); value
+//          blocks 0 and 1 of O^T come from an O^T warp, blocks 2 and 3 from the producer
+//          warp, just before it waits for the page's slot to refill it (the softmax warps
+//          are the busiest role there, and twelve warps keep ~170 registers per thread)
 template <bool kFp8>
 struct Roles {
-  static constexpr int kMmaWarps = kFp8 ? 3 : 2;
+  static constexpr int kSWarps = kFp8 ? 2 : 3;
+  static constexpr int kOWarps = kFp8 ? 1 : 0;
+  static constexpr int kMmaWarps = kSWarps + kOWarps;
   static constexpr int kThreads = 32 * (1 + kMmaWarps + kSoftmaxWarps);
 };
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;       // O^T block b at columns 64 b (N <= 64)
-constexpr uint32_t kTmemS = 256;     // S^T buffer b, partial p at columns 256 + 128 b + 64 p
+// S^T: bf16: one buffer, partial p of the three at columns 256 + 64 p (N <= 48);
+//       e4m3: two buffers, buffer b at columns 256 + 128 b (Q_hi and Q_lo products, 2 N <= 96)
+constexpr uint32_t kTmemS = 256;
 constexpr float kRefSlack = 8.0f;    // octaves a score may exceed the row reference before it moves
 // e4m3 path: a smaller slack (p <= 16) so that P can be stored times 2^4 (<= 256 < 448,
 // the largest e4m3); probabilities down to 2^-10 of the reference stay in e4m3's normal
@@ -129,6 +141,7 @@ constexpr float kRefSlack = 8.0f;    // octaves a score may exceed the row refer
 constexpr float kRefSlackFp8 = 4.0f;
 constexpr float kPShiftFp8 = 4.0f;
 constexpr long long kWaitBudget = 2000000000LL;  // cycles (~1 s) before a wait gives up
+constexpr long long kWaitBudgetTest = 4000000LL; // ~2 ms: the budget of a call that tests the timeout path
 
 struct Params {
   const PlanUnit* units;   // the plan's unit table (one record per CTA)
@@ -142,9 +155,11 @@ struct Params {
   float out_scale;         // kv_scale (1 for a bf16 cache)
   __nv_bfloat16* out;
   float* lse;
-  float* part_o;
+  __nv_bfloat16* part_o;  // split partials of O (bf16, each normalised by its split's l)
   float* part_lse;
   int32_t* status;
+  long long wait_budget;  // cycles a bounded wait may take (kWaitBudget; kWaitBudgetTest in a timeout test)
+  int skip_copy;          // page of the first unit whose copy is never issued (timeout test), or -1
 };
 
 struct Misc {
@@ -152,7 +167,7 @@ struct Misc {
   uint64_t kv_full[4], kv_empty[4];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], pt_empty[2];  // p_full: e4m3 only (the O^T warp waits on it)
-  uint64_t mma_done[8];
+  uint64_t mma_done[8];  // MMA warps 0..2, producer 3, softmax O^T issuers 4..7
   uint32_t tmem_base;
   int abort;
   int unit[12];  // this CTA's PlanUnit
@@ -171,24 +186,24 @@ __device__ __forceinline__ void report(int32_t* status, int bits) {
 }
 
 // Bounded wait: false when the budget ran out or another warp aborted the unit.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status) {
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort, const Params& p) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   long long t0 = clock64();
   while (true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitBudget) {
+    if (clock64() - t0 > p.wait_budget) {
       *abort = 1;
-      report(status, MLA_DEVICE_WAIT_TIMEOUT);
+      report(p.status, MLA_DEVICE_WAIT_TIMEOUT);
       return false;
     }
   }
 }
 
 // Warp-uniform bounded wait: lane 0 polls, the result is broadcast to the warp.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status) {
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, const Params& p) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort, status) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort, p) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -243,41 +258,43 @@ __device__ __forceinline__ int sw64_offset(int row, int col) {
   return row * 64 + ((((col >> 4) ^ (row >> 1)) & 3) << 4) + (col & 15);
 }
 
-// O^T += V^T . P^T(t) for value block blk (MN-major V^T from page t's ring slot, MN-major
-// P^T), issued by one lane; accumulates onto the earlier tiles.
-template <bool kFp8>
-__device__ __forceinline__ void issue_ot_block(uint32_t tmem, uint32_t skv, uint32_t spt, int t, int nmma, int blk) {
-  using G = Geo<kFp8>;
-  const uint32_t idesc_o = kFp8 ? ptx::idesc_e4m3(128, nmma, 1, 1) : ptx::idesc_bf16(128, nmma, 1, 1);
+// O^T is zeroed in tensor memory before the first tile, so every O^T MMA accumulates and
+// the MMAs of one value block may come from different threads in any order.
+// bf16: O^T += V^T . P^T(t) for value block blk (MN-major V^T from page t's ring slot,
+// MN-major P^T), the block's four K-steps, issued by one lane.
+__device__ __forceinline__ void issue_ot_block_bf16(uint32_t tmem, uint32_t skv, uint32_t spt, int t, int nmma,
+                                                    int blk) {
+  using G = Geo<false>;
+  const uint32_t idesc_o = ptx::idesc_bf16(128, nmma, 1, 1);
   const uint32_t pt0 = spt + (t & 1) * kPtBytes;
   // value columns [128 blk, 128 blk + 128) = chunks 2 blk, 2 blk + 1 of the page
   const uint32_t v0 = skv + (t % G::kStages) * G::kSlot + 2 * blk * G::kChunkBytes;
   const uint32_t d = tmem + kTmemO + 64 * blk;
-  if constexpr (kFp8) {
-    // K = 32 keys per MMA; P^T = hi + lo parts (64 keys x 64 bytes each)
 #pragma unroll
-    for (int k = 0; k < 2; ++k)
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        uint64_t ad = ptx::smem_desc(v0 + 2048 * k, G::kChunkBytes, 512, ptx::kSwizzle64B);
-        uint64_t bd = ptx::smem_desc(pt0 + part * (kTileKeys * 64) + 2048 * k, 4096, 512, ptx::kSwizzle64B);
-        ptx::mma_e4m3_ss(d, ad, bd, idesc_o, (t > 0 || k > 0 || part > 0) ? 1u : 0u);
-      }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint64_t ad = ptx::smem_desc(v0 + 2048 * k, G::kChunkBytes, 1024, ptx::kSwizzle128B);
-      uint64_t bd = ptx::smem_desc(pt0 + 2048 * k, 8192, 1024, ptx::kSwizzle128B);
-      ptx::mma_bf16_ss(d, ad, bd, idesc_o, (t > 0 || k > 0) ? 1u : 0u);
-    }
+  for (int k = 0; k < 4; ++k) {
+    uint64_t ad = ptx::smem_desc(v0 + 2048 * k, G::kChunkBytes, 1024, ptx::kSwizzle128B);
+    uint64_t bd = ptx::smem_desc(pt0 + 2048 * k, 8192, 1024, ptx::kSwizzle128B);
+    ptx::mma_bf16_ss(d, ad, bd, idesc_o, 1u);
   }
+}
+// e4m3: one MMA of O^T += V^T . P^T(t): value block blk, K-step k (32 keys), P^T part
+// (0 = hi, 1 = lo; each 64 keys x 64 bytes).
+__device__ __forceinline__ void issue_ot_mma_e4m3(uint32_t tmem, uint32_t skv, uint32_t spt, int t, int nmma, int blk,
+                                                  int k, int part) {
+  using G = Geo<true>;
+  const uint32_t idesc_o = ptx::idesc_e4m3(128, nmma, 1, 1);
+  const uint32_t pt0 = spt + (t & 1) * kPtBytes;
+  const uint32_t v0 = skv + (t % G::kStages) * G::kSlot + 2 * blk * G::kChunkBytes;
+  const uint64_t ad = ptx::smem_desc(v0 + 2048 * k, G::kChunkBytes, 512, ptx::kSwizzle64B);
+  const uint64_t bd = ptx::smem_desc(pt0 + part * (kTileKeys * 64) + 2048 * k, 4096, 512, ptx::kSwizzle64B);
+  ptx::mma_e4m3_ss(tmem + kTmemO + 64 * blk, ad, bd, idesc_o, 1u);
 }
 
 // Waits (bounded) until the tcgen05 operations this lane issued have completed.
-__device__ __forceinline__ void drain_mmas(uint64_t* done) {
+__device__ __forceinline__ void drain_mmas(uint64_t* done, long long budget) {
   ptx::mma_commit(done);
   long long t0c = clock64();
-  while (!ptx::mbar_try_wait(done, 0) && clock64() - t0c < kWaitBudget) {
+  while (!ptx::mbar_try_wait(done, 0) && clock64() - t0c < budget) {
   }
 }
 
@@ -316,6 +333,17 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
     // the device lengths differ from those the plan was built for: stop the unit
     report(p.status, MLA_DEVICE_PLAN_MISMATCH);
     *a.abort = 1;
+  }
+  {
+    // O^T starts at zero (every O^T MMA accumulates): this warp clears the lanes of its
+    // quadrant in columns [128 grp, 128 grp + 128) of the O^T region
+    float z[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) z[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) ptx::tmem_st16(a.tmem + kTmemO + lane_off + 128 * grp + 16 * c, z);
+    ptx::tmem_st_wait();
+    ptx::tc_fence_before();
   }
   if (sidx < 64) {
     int lim = 0;
@@ -391,21 +419,30 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
     float x[NC];
     bool need = false;
     bool unmasked = false;  // this tile: every key visible to every row
-    if (!fail) fail = !warp_wait(&ms->s_full[sb], (t >> 1) & 1, abort, p.status);
+    // S^T(t): e4m3 buffer t % 2; bf16 the one buffer (its phase flips every tile)
+    const int s_buf = kFp8 ? sb : 0;
+    if (!fail) fail = !warp_wait(&ms->s_full[s_buf], kFp8 ? ((t >> 1) & 1) : (t & 1), abort, p);
     if (!fail) {
       ptx::tc_fence_after();
-      // S^T = the sum of two accumulator column blocks (bf16: the two partials; e4m3: the
-      // Q_hi and Q_lo products); lanes 0..15 read 8 columns, lanes 16..31 take 4 of them
-      const uint32_t sbase = a.tmem + kTmemS + 128 * sb + lane_off + 8 * grp;
-      constexpr uint32_t kSecond = kFp8 ? 16 * NCH : 64;
+      // S^T: e4m3: the sum of the Q_hi and Q_lo column blocks of buffer t % 2; bf16: the
+      // sum of the three partials. Lanes 0..15 read 8 columns, lanes 16..31 take 4 of them
+      const uint32_t sbase = a.tmem + kTmemS + (kFp8 ? 128 * sb : 0) + lane_off + 8 * grp;
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         float s0[8], s1[8];
         ptx::tmem_ld8(sbase + 16 * c, s0);
-        ptx::tmem_ld8(sbase + kSecond + 16 * c, s1);
-        ptx::tmem_ld_wait();
+        ptx::tmem_ld8(sbase + (kFp8 ? 16 * NCH : 64) + 16 * c, s1);
+        if constexpr (kFp8) {
+          ptx::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) s0[j] += s1[j];
+          for (int j = 0; j < 8; ++j) s0[j] += s1[j];
+        } else {
+          float s2[8];
+          ptx::tmem_ld8(sbase + 128 + 16 * c, s2);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) s0[j] = (s0[j] + s1[j]) + s2[j];
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float hi = __shfl_sync(0xffffffffu, s0[4 + j], lane & 15);
@@ -414,7 +451,7 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&ms->s_empty[sb]);
+      if (lane == 0) ptx::mbar_arrive(&ms->s_empty[s_buf]);
       const int key = a.kv_begin + t * kTileKeys + krow;
       const int tile_last = a.kv_begin + t * kTileKeys + kTileKeys - 1;
       unmasked = tile_last < a.kv_end && tile_last < lim_min;  // tile-uniform fast path
@@ -459,7 +496,7 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
       for (int i = 0; i < NC; ++i) l_acc[i] *= ms->alpha[16 * (i / 4) + col0 + (i % 4)];
       if (t >= 1) {
         // this warp: value blocks 2 grp and 2 grp + 1 of its lane quadrant
-        fail = !warp_wait(&ms->pt_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, p.status);
+        fail = !warp_wait(&ms->pt_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, p);
         if (!fail) {
           ptx::tc_fence_after();
 #pragma unroll 1
@@ -561,7 +598,7 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
       }
       if (!fail) {
         make_p();
-        if (t >= 2) fail = !warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p.status);
+        if (t >= 2) fail = !warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p);
       }
       if (!fail) {
 #pragma unroll
@@ -579,7 +616,7 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
     // one value block of O^T(t) and release the page slot and the P^T buffer.
     if (!fail) {
       make_p();
-      if (t >= 2) fail = !warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p.status);
+      if (t >= 2) fail = !warp_wait(&ms->pt_empty[sb], ((t - 2) >> 1) & 1, abort, p);
     }
     if (!fail) store_p();
     if (softmax_any(need || fail || *abort != 0)) {
@@ -602,7 +639,7 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
     if (w8 < 4) {
       ptx::tc_fence_after();
       if (lane == 0) {
-        issue_ot_block<kFp8>(a.tmem, a.skv, a.spt, t, a.nmma, w8);
+        issue_ot_block_bf16(a.tmem, a.skv, a.spt, t, a.nmma, w8);
         ptx::mma_commit(&ms->kv_empty[t % G::kStages]);
         ptx::mma_commit(&ms->pt_empty[sb]);
         issued_ot = true;
@@ -611,36 +648,40 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
     }
   }
   // ------------------------------------------------------------ epilogue
+  // Row sums, LSE and the per-row output scale first: they need only l, so they overlap
+  // the last tile's O^T MMAs. The wait for those MMAs and the abort vote come after.
   if (!stop) {
-    if (!fail) fail = !warp_wait(&ms->pt_empty[(a.ntiles - 1) & 1], ((a.ntiles - 1) >> 1) & 1, abort, p.status);
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+      float s = l_acc[i];
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if ((lane & 15) == 0) ms->colred[qd][16 * (i / 4) + col0 + (i % 4)] = s;
+    }
+    softmax_sync();
+    if (sidx < 64) {
+      float L = 0.f;
+      if (sidx < a.nrows) {
+        L = ms->colred[0][sidx] + ms->colred[1][sidx] + ms->colred[2][sidx] + ms->colred[3][sidx];
+        const float lse_v = L > 0.f ? (ms->ref[sidx] + lg2(L)) * 0.69314718055994531f : -INFINITY;
+        if (a.part_row0 < 0) {
+          if (p.lse) p.lse[a.qrow0 + sidx] = lse_v;
+        } else {
+          p.part_lse[a.part_row0 + sidx] = lse_v;
+        }
+      }
+      ms->oscale[sidx] = L > 0.f ? p.out_scale / L : 0.f;  // one division per row
+    }
+    if (!fail) fail = !warp_wait(&ms->pt_empty[(a.ntiles - 1) & 1], ((a.ntiles - 1) >> 1) & 1, abort, p);
+    // this barrier also publishes oscale to all softmax warps
     stop = softmax_any(fail || *abort != 0);
   }
   if (stop) return issued_ot;
   ptx::tc_fence_after();
-#pragma unroll
-  for (int i = 0; i < NC; ++i) {
-    float s = l_acc[i];
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if ((lane & 15) == 0) ms->colred[qd][16 * (i / 4) + col0 + (i % 4)] = s;
-  }
-  softmax_sync();
-  if (sidx < 64) {
-    float L = 0.f;
-    if (sidx < a.nrows) {
-      L = ms->colred[0][sidx] + ms->colred[1][sidx] + ms->colred[2][sidx] + ms->colred[3][sidx];
-      const float lse_v = L > 0.f ? (ms->ref[sidx] + lg2(L)) * 0.69314718055994531f : -INFINITY;
-      if (a.part_row0 < 0) {
-        if (p.lse) p.lse[a.qrow0 + sidx] = lse_v;
-      } else {
-        p.part_lse[a.part_row0 + sidx] = lse_v;
-      }
-    }
-    ms->oscale[sidx] = L > 0.f ? p.out_scale / L : 0.f;  // one division per row
-  }
-  softmax_sync();
   // O^T(dv, row) / l(row): this thread holds dv = 128 blk + 32 qd + lane of value blocks
-  // 2 grp, 2 grp + 1; a warp's stores of one row cover 32 consecutive dv
+  // 2 grp, 2 grp + 1; a warp's stores of one row cover 32 consecutive dv (bf16 out, or
+  // the bf16 split partial)
+  __nv_bfloat16* dst = a.part_row0 < 0 ? p.out + (size_t)a.qrow0 * kDv : p.part_o + (size_t)a.part_row0 * kDv;
   const int dv_in_blk = qd * 32 + lane;
 #pragma unroll 1
   for (int blk = 2 * grp; blk < 2 * grp + 2; ++blk) {
@@ -658,12 +699,7 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int n = 16 * c + j + u;
-          if (n < a.nrows) {
-            if (a.part_row0 < 0)
-              p.out[(size_t)(a.qrow0 + n) * kDv + dv] = __float2bfloat16_rn(v4[u]);
-            else
-              p.part_o[(size_t)(a.part_row0 + n) * kDv + dv] = v4[u];
-          }
+          if (n < a.nrows) dst[(size_t)n * kDv + dv] = __float2bfloat16_rn(v4[u]);
         }
       }
     }
@@ -698,14 +734,15 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
     if (lane == 0) {
       ms->abort = 0;
       ptx::mbar_init(&ms->bar_q, kFp8 ? kSoftmaxWarps : 1);  // e4m3: the softmax warps convert Q themselves
+    constexpr int kOtIssuers = kFp8 ? 2 : 4;  // e4m3: the O^T warp and the producer; bf16: four softmax warps
     for (int i = 0; i < 4; ++i) {
       ptx::mbar_init(&ms->kv_full[i], 1);
-      ptx::mbar_init(&ms->kv_empty[i], kFp8 ? 1 : 4);  // the O^T issuer(s)
+      ptx::mbar_init(&ms->kv_empty[i], kOtIssuers);
     }
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&ms->s_full[i], kFp8 ? 1 : 2);  // the S^T warp(s) of a tile
+      ptx::mbar_init(&ms->s_full[i], kFp8 ? 1 : Roles<kFp8>::kSWarps);  // the S^T warp(s) of a tile
       ptx::mbar_init(&ms->s_empty[i], kSoftmaxWarps);
-      ptx::mbar_init(&ms->pt_empty[i], kFp8 ? 1 : 4);
+      ptx::mbar_init(&ms->pt_empty[i], kOtIssuers);
       ptx::mbar_init(&ms->p_full[i], kSoftmaxWarps);
     }
     for (int i = 0; i < 8; ++i) ptx::mbar_init(&ms->mma_done[i], 1);
@@ -747,6 +784,7 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     int issued = 0;
+    bool ot_issued = false;  // e4m3: lane 0 issued O^T MMAs
     const bool q_issued = !kFp8;
     {
       const int32_t* pt_row = p.page_table + (size_t)b * p.pt_stride + kv_begin / kPage;
@@ -764,6 +802,26 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
         return pid;
       };
       auto load_ids = [&](int t0) { return checked(t0 + lane < ntiles ? pt_row[t0 + lane] : 0, t0 + lane); };
+      // e4m3 (lane 0): O^T(u) += V^T . P^T(u) for value blocks 2 and 3, once P^T(u) is written
+      auto producer_ot = [&](int u) -> int {
+        if (!wait_bar(&ms->p_full[u & 1], (u >> 1) & 1, abort, p)) return 0;
+        ptx::tc_fence_after();
+        const uint32_t skv = ptx::smem_addr(sKv), spt = ptx::smem_addr(sPt);
+#pragma unroll
+        for (int blk = 2; blk < 4; ++blk)
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+#pragma unroll
+            for (int part = 0; part < 2; ++part) issue_ot_mma_e4m3(tmem, skv, spt, u, nmma, blk, k, part);
+        ptx::mma_commit(&ms->kv_empty[u % S]);
+        ptx::mma_commit(&ms->pt_empty[u & 1]);
+        ot_issued = true;
+        return 1;
+      };
+      // a page that only this row tile reads may leave L2 first once it is in shared
+      // memory, which keeps the plan, the page table and the split partials there
+      const bool read_once = (ms->unit[11] & kUnitKvReadOnce) != 0;
+      const uint64_t pol = ptx::policy_evict_first();
       pid_cur = checked(pid_cur, lane);
       pid_next = checked(pid_next, 32 + lane);
       for (int t0 = 0; t0 < ntiles && !*abort; t0 += 32) {
@@ -775,10 +833,16 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
           const int t = t0 + i, slot = t % S;
           int ok = 1;
           if (lane == 0) {
-            if (t >= S) ok = wait_bar(&ms->kv_empty[slot], ((t - S) / S) & 1, abort, p.status);
-            if (ok) {
+            // e4m3: this warp also issues value blocks 2 and 3 of O^T(t - S), the page whose
+            // slot the copy of page t reuses (blocks 0 and 1 come from the O^T warp)
+            if (kFp8 && t >= S) ok = producer_ot(t - S);
+            if (ok && t >= S) ok = wait_bar(&ms->kv_empty[slot], ((t - S) / S) & 1, abort, p);
+            if (ok && !(blockIdx.x == 0 && t == p.skip_copy)) {
               ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], G::kSlot);
-              ptx::tma_load_3d(sKv + slot * G::kSlot, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0);
+              if (read_once)
+                ptx::tma_load_3d_hint(sKv + slot * G::kSlot, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0, pol);
+              else
+                ptx::tma_load_3d(sKv + slot * G::kSlot, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0);
               if ((kFp8 || t >= S) && t0 + tp < ntiles) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, page_pf * kPage, 0);
             }
           }
@@ -791,7 +855,7 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
             int pf[S];
 #pragma unroll
             for (int k = 0; k < S; ++k) pf[k] = __shfl_sync(0xffffffffu, pid_cur, S + k);
-            if (lane == 0 && wait_bar(&ms->kv_full[0], 0, abort, p.status)) {
+            if (lane == 0 && wait_bar(&ms->kv_full[0], 0, abort, p)) {
 #pragma unroll
               for (int k = 0; k < S; ++k)
                 if (S + k < ntiles) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, pf[k] * kPage, 0);
@@ -801,77 +865,99 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
         pid_cur = pid_next;
         pid_next = (t0 + 64 < ntiles) ? load_ids(t0 + 64) : 0;
       }
+      // e4m3: blocks 2 and 3 of O^T for the last S pages (no copy follows them)
+      if (kFp8 && issued == ntiles) {
+        int ok = 1;
+        if (lane == 0)
+          for (int u = max(0, ntiles - S); ok && u < ntiles; ++u) ok = producer_ot(u);
+        __syncwarp();
+      }
     }
     // Drain: every issued copy must land before the CTA may exit (at most the last S
     // pages can still be in flight; earlier ones were consumed by the MMAs).
     if (lane == 0) {
       for (int t = max(0, issued - S); t < issued; ++t) {
+        if (blockIdx.x == 0 && t == p.skip_copy) continue;  // never issued (timeout test)
         long long t0c = clock64();
-        while (!ptx::mbar_try_wait(&ms->kv_full[t % S], (t / S) & 1) && clock64() - t0c < kWaitBudget) {
+        while (!ptx::mbar_try_wait(&ms->kv_full[t % S], (t / S) & 1) && clock64() - t0c < p.wait_budget) {
         }
       }
       if (q_issued) {
         long long t0c = clock64();
-        while (!ptx::mbar_try_wait(&ms->bar_q, 0) && clock64() - t0c < kWaitBudget) {
+        while (!ptx::mbar_try_wait(&ms->bar_q, 0) && clock64() - t0c < p.wait_budget) {
         }
       }
+      // and the O^T MMAs this lane issued must retire before TMEM is released
+      if (ot_issued) drain_mmas(&ms->mma_done[3], p.wait_budget);
     }
+    __syncwarp();
   } else if (warp <= Roles<kFp8>::kMmaWarps) {
     // ------------------------------------------------------------ MMA issue
+    // One thread issues a tcgen05.mma only every ~100 cycles, so several warps issue the
+    // products of a page, each into accumulators that no other thread writes.
+    const int mi = warp - 1;
     const uint32_t sq = ptx::smem_addr(sQ), skv = ptx::smem_addr(sKv), spt = ptx::smem_addr(sPt);
-    bool ok = !*abort && warp_wait(&ms->bar_q, 0, abort, p.status);
+    bool ok = !*abort && warp_wait(&ms->bar_q, 0, abort, p);
     bool issued = false;
-    if (warp <= 2) {
-      // S^T(t) = K . Q^T into buffer t % 2 (K-major K tile, K-major Q). bf16: warp 1 + pw
-      // accumulates partial pw of every tile. e4m3: warp 1 + pw issues the tiles with
-      // t % 2 == pw, all 18 K-steps, N = 2 nmma (Q_hi and Q_lo side by side).
-      const int pw = warp - 1;
+    if (mi < Roles<kFp8>::kSWarps) {
       const uint32_t idesc_s = kFp8 ? ptx::idesc_e4m3(64, 2 * nmma, 0, 0) : ptx::idesc_bf16(64, nmma, 0, 0);
       for (int t = 0; ok && t < ntiles; ++t) {
-        if (kFp8 && (t & 1) != pw) continue;
-        ok = warp_wait(&ms->kv_full[t % S], (t / S) & 1, abort, p.status);
-        // the softmax must have read S^T(t - 2) out of this buffer
-        if (ok && t >= 2) ok = warp_wait(&ms->s_empty[t & 1], ((t - 2) >> 1) & 1, abort, p.status);
+        // e4m3: warp mi takes the pages with t % 2 == mi; bf16: every page
+        if (kFp8 && (t & 1) != mi) continue;
+        ok = warp_wait(&ms->kv_full[t % S], (t / S) & 1, abort, p);
+        // the softmax must have read the previous S^T out of this buffer (e4m3: of t - 2 in
+        // buffer t % 2; bf16: of t - 1 in the one buffer)
+        if constexpr (kFp8) {
+          if (ok && t >= 2) ok = warp_wait(&ms->s_empty[t & 1], ((t - 2) >> 1) & 1, abort, p);
+        } else {
+          if (ok && t >= 1) ok = warp_wait(&ms->s_empty[0], (t - 1) & 1, abort, p);
+        }
         if (!ok) break;
         ptx::tc_fence_after();
         if (lane == 0) {
           const uint32_t a0 = skv + (t % S) * G::kSlot;
           if constexpr (kFp8) {
+            // S^T(t) = K . [Q_hi | Q_lo]^T into buffer t % 2: all 18 K-steps (32 columns each)
             const uint32_t d = tmem + kTmemS + 128 * (t & 1);
 #pragma unroll
             for (int ks = 0; ks < 18; ++ks) {
               const int c = ks >> 1, kk = ks & 1;
-              uint64_t ad = ptx::smem_desc(a0 + c * G::kChunkBytes + 32 * kk, 16, 512, ptx::kSwizzle64B);
-              uint64_t bd = ptx::smem_desc(sq + c * kQ8ChunkBytes + 32 * kk, 16, 512, ptx::kSwizzle64B);
+              const uint64_t ad = ptx::smem_desc(a0 + c * G::kChunkBytes + 32 * kk, 16, 512, ptx::kSwizzle64B);
+              const uint64_t bd = ptx::smem_desc(sq + c * kQ8ChunkBytes + 32 * kk, 16, 512, ptx::kSwizzle64B);
               ptx::mma_e4m3_ss(d, ad, bd, idesc_s, ks != 0 ? 1u : 0u);
             }
+            ptx::mma_commit(&ms->s_full[t & 1]);
           } else {
-            const uint32_t d = tmem + kTmemS + 128 * (t & 1) + 64 * pw;
-            // partial pw = K-steps [18 pw, 18 pw + 18) of the 36 (16 columns each)
+            // partial mi of S^T(t) = K . Q^T: K-steps [12 mi, 12 mi + 12) of the 36 (16 columns each)
+            const uint32_t d = tmem + kTmemS + 64 * mi;
 #pragma unroll
-            for (int i = 0; i < 18; ++i) {
-              const int ks = 18 * pw + i, c = ks >> 2, k = ks & 3;
-              uint64_t ad = ptx::smem_desc(a0 + c * G::kChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
-              uint64_t bd = ptx::smem_desc(sq + c * kQChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
+            for (int i = 0; i < 12; ++i) {
+              const int ks = 12 * mi + i, c = ks >> 2, k = ks & 3;
+              const uint64_t ad = ptx::smem_desc(a0 + c * G::kChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
+              const uint64_t bd = ptx::smem_desc(sq + c * kQChunkBytes + 32 * k, 16, 1024, ptx::kSwizzle128B);
               ptx::mma_bf16_ss(d, ad, bd, idesc_s, i != 0 ? 1u : 0u);
             }
+            ptx::mma_commit(&ms->s_full[0]);
           }
-          ptx::mma_commit(&ms->s_full[t & 1]);
         }
         __syncwarp();
         issued = true;
       }
-    }
-    if (kFp8 && warp == 3) {
-      // e4m3: O^T(t) += V^T . P^T(t), all four value blocks, once the softmax warps have
-      // written P^T(t)
+    } else if constexpr (kFp8) {
+      // e4m3: O^T(t) += V^T . P^T(t) for value blocks 0 and 1 (the producer issues 2 and 3),
+      // once the softmax warps have written P^T(t)
+      const int ow = mi - Roles<kFp8>::kSWarps;  // 0
       for (int t = 0; ok && t < ntiles; ++t) {
-        ok = warp_wait(&ms->p_full[t & 1], (t >> 1) & 1, abort, p.status);
+        ok = warp_wait(&ms->p_full[t & 1], (t >> 1) & 1, abort, p);
         if (!ok) break;
         ptx::tc_fence_after();
         if (lane == 0) {
 #pragma unroll
-          for (int blk = 0; blk < 4; ++blk) issue_ot_block<kFp8>(tmem, skv, spt, t, nmma, blk);
+          for (int blk = 2 * ow; blk < 2 * ow + 2; ++blk)
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+#pragma unroll
+              for (int part = 0; part < 2; ++part) issue_ot_mma_e4m3(tmem, skv, spt, t, nmma, blk, k, part);
           ptx::mma_commit(&ms->kv_empty[t % S]);
           ptx::mma_commit(&ms->pt_empty[t & 1]);
         }
@@ -881,7 +967,7 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
     }
     // every MMA this warp issued must retire before TMEM is released
     if (issued) {
-      if (lane == 0) drain_mmas(&ms->mma_done[warp - 1]);
+      if (lane == 0) drain_mmas(&ms->mma_done[mi], p.wait_budget);
       __syncwarp();
     }
   } else {
@@ -898,7 +984,7 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
     else
       issued_ot = softmax_role<3, kFp8>(a, p);
     // the O^T MMAs this lane issued must retire before TMEM is released
-    if (issued_ot) drain_mmas(&ms->mma_done[3 + (warp - 1 - kMma)]);
+    if (issued_ot) drain_mmas(&ms->mma_done[4 + (warp - 1 - kMma)], p.wait_budget);
     __syncwarp();
   }
 
@@ -913,19 +999,26 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
 // ------------------------------------------------------------------ LSE merge
 // One CTA per (packed row, quarter of the 512 value columns): its W warps (4, 8 or 16,
 // enough for all splits at kMergeBatch loads per lane) share the splits of the row; fewer
-// warps per CTA let more CTAs share an SM. L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s; a split that
-// a causal row cannot see has L_s = -inf and weight 0. The first batch of partial-O
-// loads is issued before the LSE reduction, so that both wait on memory together.
+// warps per CTA let more CTAs share an SM. L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s.
 constexpr int kMergeThreads = 512;
 constexpr int kMergeWarps = kMergeThreads / 32;
 constexpr int kMergeBatch = 10;  // partial-O loads in flight per lane (16 warps x 10 = 160 splits per round trip)
 constexpr int kMergeMaxSplits = 2048;
 
+// Four bf16 partial-O values (8 bytes, streamed: read once) as fp32.
+__device__ __forceinline__ float4 load_part4(const __nv_bfloat16* ptr) {
+  const uint2 raw = __ldcs(reinterpret_cast<const uint2*>(ptr));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// 64 registers per thread (the minimum-blocks bound): two 16-warp CTAs per SM, so the
+// merge CTAs of a 48-row tile with ~150 splits (192 of them) run in one wave.
 template <int W>
-__global__ void __launch_bounds__(32 * W) lse_merge_kernel(const PlanMerge* merges, const float* part_o,
+__global__ void __launch_bounds__(32 * W, 1024 / (32 * W)) lse_merge_kernel(const PlanMerge* merges, const __nv_bfloat16* part_o,
                                                                  const float* part_lse, __nv_bfloat16* out, float* lse) {
-  __shared__ float w_s[kMergeMaxSplits];
-  __shared__ float red[W][2];
+  __shared__ float m_s[W], l_s[W];
   __shared__ float4 acc_s[W][32];
   // the merge item is plan data, written before the fold kernel ran: read it while the
   // fold kernel finishes, then wait for the partials
@@ -934,82 +1027,66 @@ __global__ void __launch_bounds__(32 * W) lse_merge_kernel(const PlanMerge* merg
   const int row = blockIdx.x >> 2, quarter = blockIdx.x & 3;
   if (row >= m.nrows) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int nw = W, nt = 32 * W;  // warps: chosen by the host for the split count
   const int ns = m.n_splits;  // the planner keeps this <= kMergeMaxSplits
   const int col = quarter * 128 + 4 * lane;
-  const float* base = part_o + (size_t)(m.part_row0 + row) * kDv + col;
+  const __nv_bfloat16* base = part_o + (size_t)(m.part_row0 + row) * kDv + col;
   const size_t split_stride = (size_t)m.nrows * kDv;
-  float4 v[kMergeBatch];
-#pragma unroll
-  for (int u = 0; u < kMergeBatch; ++u) {
-    const int s = warp + nw * u;
-    v[u] = s < ns ? __ldcs(reinterpret_cast<const float4*>(base + (size_t)s * split_stride)) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  // 1. L over the splits
-  float mx = -INFINITY;
-  for (int s = threadIdx.x; s < ns; s += nt) {
-    const float x = part_lse[m.part_row0 + s * m.nrows + row];
-    w_s[s] = x;
-    mx = fmaxf(mx, x);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) red[warp][0] = mx;
-  __syncthreads();
-  mx = red[0][0];
-#pragma unroll
-  for (int i = 1; i < W; ++i) mx = fmaxf(mx, red[i][0]);
-  float sum = 0.f;
-  for (int s = threadIdx.x; s < ns; s += nt) {
-    const float x = w_s[s];
-    sum += x == -INFINITY ? 0.f : __expf(x - mx);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane == 0) red[warp][1] = sum;
-  __syncthreads();
-  sum = 0.f;
-#pragma unroll
-  for (int i = 0; i < W; ++i) sum += red[i][1];
-  const float L = mx + __logf(sum);
-  for (int s = threadIdx.x; s < ns; s += nt) {
-    const float x = w_s[s];
-    w_s[s] = x == -INFINITY ? 0.f : __expf(x - L);
-  }
-  __syncthreads();
-  // 2. weighted sum: warp w takes splits w, w + 16, ...; each lane 4 consecutive columns
+  // Warp w folds its splits w, w + W, ... into a running (max M_w, sum l_w = sum_s e^(L_s -
+  // M_w), acc_w = sum_s e^(L_s - M_w) O_s), kMergeBatch splits per round trip (their
+  // partial O and LSE loads issued together); one barrier then combines the W warps:
+  // L = M + ln l, O = acc / l. A split that the row cannot see has L_s = -inf: weight 0.
+  float mw = -INFINITY, lw = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0;;) {
+  for (int s0 = warp; s0 < ns; s0 += W * kMergeBatch) {
+    uint2 v[kMergeBatch];  // four bf16 partial-O values each, unpacked when used
+    float x[kMergeBatch];
 #pragma unroll
     for (int u = 0; u < kMergeBatch; ++u) {
-      const int s = s0 + warp + nw * u;
-      if (s < ns) {
-        const float w = w_s[s];
-        acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;
-      }
+      const int s = s0 + W * u;
+      v[u] = s < ns ? __ldcs(reinterpret_cast<const uint2*>(base + (size_t)s * split_stride)) : make_uint2(0u, 0u);
+      x[u] = s < ns ? part_lse[m.part_row0 + s * m.nrows + row] : -INFINITY;
     }
-    s0 += nw * kMergeBatch;
-    if (s0 >= ns) break;
+    float mb = mw;
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) mb = fmaxf(mb, x[u]);
+    if (mb == -INFINITY) continue;  // nothing visible so far
+    const float sc = mw == -INFINITY ? 0.f : __expf(mw - mb);
+    lw *= sc;
+    acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
 #pragma unroll
     for (int u = 0; u < kMergeBatch; ++u) {
-      const int s = s0 + warp + nw * u;
-      v[u] = s < ns ? __ldcs(reinterpret_cast<const float4*>(base + (size_t)s * split_stride))
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float w = x[u] == -INFINITY ? 0.f : __expf(x[u] - mb);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[u].x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[u].y));
+      lw += w;
+      acc.x += w * a.x; acc.y += w * a.y; acc.z += w * b.x; acc.w += w * b.y;
     }
+    mw = mb;
+  }
+  if (lane == 0) {
+    m_s[warp] = mw;
+    l_s[warp] = lw;
   }
   acc_s[warp][lane] = acc;
   __syncthreads();
   if (warp == 0) {
-    float4 r = acc_s[0][lane];
+    float M = m_s[0];
 #pragma unroll
-    for (int i = 1; i < W; ++i) {
-      const float4 x = acc_s[i][lane];
-      r.x += x.x; r.y += x.y; r.z += x.z; r.w += x.w;
+    for (int i = 1; i < W; ++i) M = fmaxf(M, m_s[i]);
+    float l = 0.f;
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      const float f = m_s[i] == -INFINITY ? 0.f : __expf(m_s[i] - M);
+      const float4 a = acc_s[i][lane];
+      l += f * l_s[i];
+      r.x += f * a.x; r.y += f * a.y; r.z += f * a.z; r.w += f * a.w;
     }
+    const float inv = 1.f / l;
     const int qr = m.qrow0 + row;
-    uint2 pk = make_uint2(pack_bf16(r.x, r.y), pack_bf16(r.z, r.w));
-    *reinterpret_cast<uint2*>(out + (size_t)qr * kDv + col) = pk;
-    if (lse && quarter == 0 && lane == 0) lse[qr] = L;
+    *reinterpret_cast<uint2*>(out + (size_t)qr * kDv + col) =
+        make_uint2(pack_bf16(r.x * inv, r.y * inv), pack_bf16(r.z * inv, r.w * inv));
+    if (lse && quarter == 0 && lane == 0) lse[qr] = M + __logf(l);
   }
 }
 
@@ -1021,7 +1098,7 @@ constexpr int kMergeSmallSplits = 16;
 constexpr int kMergeSmallWarps = 8;
 
 __global__ void __launch_bounds__(32 * kMergeSmallWarps) lse_merge_small_kernel(const PlanMerge* merges,
-                                                                                const float* part_o,
+                                                                                const __nv_bfloat16* part_o,
                                                                                 const float* part_lse,
                                                                                 __nv_bfloat16* out, float* lse) {
   const PlanMerge m = merges[blockIdx.y];  // plan data: read before the wait, as above
@@ -1032,13 +1109,12 @@ __global__ void __launch_bounds__(32 * kMergeSmallWarps) lse_merge_small_kernel(
   if (row >= m.nrows) return;
   const int ns = m.n_splits;  // <= kMergeSmallSplits (checked on the host)
   const int col = quarter * 128 + 4 * lane;
-  const float* base = part_o + (size_t)(m.part_row0 + row) * kDv + col;
+  const __nv_bfloat16* base = part_o + (size_t)(m.part_row0 + row) * kDv + col;
   const size_t split_stride = (size_t)m.nrows * kDv;
   float4 v[kMergeSmallSplits];
 #pragma unroll
   for (int s = 0; s < kMergeSmallSplits; ++s)
-    v[s] = s < ns ? __ldcs(reinterpret_cast<const float4*>(base + (size_t)s * split_stride))
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[s] = s < ns ? load_part4(base + (size_t)s * split_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
   const float x = lane < ns ? part_lse[m.part_row0 + lane * m.nrows + row] : -INFINITY;
   float mx = x;
 #pragma unroll
@@ -1194,10 +1270,12 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
   prm.out_scale = ks;
   prm.out = (__nv_bfloat16*)out;
   prm.lse = lse;
-  prm.part_o = (float*)workspace;
-  prm.part_lse = ws_need ? (float*)((uint8_t*)workspace + ((size_t)h->n_part_rows * kDv * sizeof(float) + 255) / 256 * 256)
-                         : nullptr;
+  prm.part_o = (__nv_bfloat16*)workspace;
+  prm.part_lse =
+      ws_need ? (float*)((uint8_t*)workspace + ((size_t)h->n_part_rows * kDv * kPartOElemBytes + 255) / 256 * 256) : nullptr;
   prm.status = status_dev;
+  prm.wait_budget = h->debug_skip_copy > 0 ? kWaitBudgetTest : kWaitBudget;
+  prm.skip_copy = h->debug_skip_copy - 1;
   cudaStream_t st = (cudaStream_t)stream;
   if (fp8)
     fold_decode_kernel<true><<<h->n_units, Roles<true>::kThreads, kSmemBytes, st>>>(tq, tkv, prm);
@@ -1229,7 +1307,7 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
                             small ? lse_merge_small_kernel
                                   : large_warps == 4 ? lse_merge_kernel<4>
                                                      : large_warps == 8 ? lse_merge_kernel<8> : lse_merge_kernel<kMergeWarps>,
-                            (const PlanMerge*)((const uint8_t*)plan_dev + h->merge_off), (const float*)prm.part_o,
+                            (const PlanMerge*)((const uint8_t*)plan_dev + h->merge_off), (const __nv_bfloat16*)prm.part_o,
                             (const float*)prm.part_lse, (__nv_bfloat16*)out, lse);
     if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "merge kernel launch: %s", cudaGetErrorString(ce));
   }

@@ -41,7 +41,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 size_t workspace_bytes_for(int n_part_rows) {
   if (n_part_rows <= 0) return 0;
-  return align_up((size_t)n_part_rows * kDv * sizeof(float), 256) + align_up((size_t)n_part_rows * sizeof(float), 256);
+  return align_up((size_t)n_part_rows * kDv * kPartOElemBytes, 256) + align_up((size_t)n_part_rows * sizeof(float), 256);
 }
 
 }  // namespace mla
@@ -70,7 +70,7 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
                        o.max_rows_per_cta);
     cap = o.max_rows_per_cta;
   }
-  if (o.force_splits < 0 || o.min_pages_per_split < 0 || o.force_fold < 0)
+  if (o.force_splits < 0 || o.min_pages_per_split < 0 || o.force_fold < 0 || o.debug_skip_copy < 0)
     return set_error(MLA_ERR_INVALID_ARG, "plan options must be >= 0");
 
   long long total_q = 0;
@@ -206,7 +206,9 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
         u.kv_begin = kb; u.kv_end = ke;
         u.part_row0 = n_split > 1 ? part0[t - g.t0] + s * tiles[t].nrows : -1;
         u.split = s; u.n_splits = n_split;
-        u.ctx = reqs[b].ctx; u.q = reqs[b].q; u.tok0 = reqs[b].tok0; u.reserved = 0;
+        u.ctx = reqs[b].ctx; u.q = reqs[b].q; u.tok0 = reqs[b].tok0;
+        // pages read by one row tile only: the request is a single fold group of one tile
+        u.flags = (reqs[b].q / reqs[b].fold == 1 && g.t1 - g.t0 == 1) ? kUnitKvReadOnce : 0;
         units.push_back(u);
       }
     }
@@ -239,6 +241,7 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
   h.rows_cap = used_cap; h.n_part_rows = part_rows; h.max_pages = max_pages;
   h.req_off = (int32_t)req_off; h.units_off = (int32_t)units_off; h.merge_off = (int32_t)merge_off;
   h.total_bytes = (int32_t)total;
+  h.debug_skip_copy = o.debug_skip_copy;
   memcpy(base, &h, sizeof h);
   memcpy(base + req_off, reqs.data(), sizeof(PlanRequest) * batch);
   if (!units.empty()) memcpy(base + units_off, units.data(), sizeof(PlanUnit) * units.size());

@@ -8,10 +8,16 @@
 namespace mla {
 
 constexpr uint32_t kPlanMagic = 0x564C4D41u;  // "AMLV"
-constexpr uint32_t kPlanVersion = 3;
+constexpr uint32_t kPlanVersion = 4;
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kPage = 64;
+// Split partials of O are stored as bf16 (each split's O is already normalised by its
+// own l, so bf16 adds at most 2^-9 relative error before the merge's weighted sum).
+constexpr int kPartOElemBytes = 2;
+// PlanUnit.flags: the request's cache pages are read by this row tile only (one fold
+// group, one tile), so a page can leave L2 right after its copy into shared memory.
+constexpr int32_t kUnitKvReadOnce = 1;
 
 struct PlanHeader {
   uint32_t magic, version;
@@ -22,7 +28,7 @@ struct PlanHeader {
   int32_t max_pages;     // pages of the longest request
   int32_t req_off, units_off, merge_off;  // byte offsets from the plan start
   int32_t total_bytes;
-  int32_t reserved;
+  int32_t debug_skip_copy;  // mla_plan_options.debug_skip_copy (0 in production plans)
 };
 static_assert(sizeof(PlanHeader) == 64, "plan header is 64 bytes");
 
@@ -43,7 +49,7 @@ struct PlanUnit {
   int32_t split;       // split index within the row tile
   int32_t n_splits;    // splits of this row tile
   int32_t ctx, q, tok0;  // the request's fields, repeated so that a CTA reads one record
-  int32_t reserved;
+  int32_t flags;         // kUnitKv* bits
 };
 static_assert(sizeof(PlanUnit) == 48, "plan unit is 48 bytes");
 

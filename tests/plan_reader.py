@@ -2,9 +2,9 @@
 import numpy as np
 
 HEADER = ["magic", "version", "batch", "num_heads", "kv_dtype", "total_q", "n_units", "n_merge", "rows_cap",
-          "n_part_rows", "max_pages", "req_off", "units_off", "merge_off", "total_bytes", "reserved"]
+          "n_part_rows", "max_pages", "req_off", "units_off", "merge_off", "total_bytes", "debug_skip_copy"]
 UNIT = ["b", "qrow0", "nrows", "kv_begin", "kv_end", "part_row0", "split", "n_splits", "ctx", "q", "tok0",
-        "reserved"]
+        "flags"]
 REQ = ["ctx", "q", "tok0", "fold"]
 MERGE = ["qrow0", "nrows", "part_row0", "n_splits"]
 

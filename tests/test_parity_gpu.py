@@ -261,3 +261,30 @@ def test_bad_page_id_is_reported_not_faulted():
     assert st2 == 0
     o_ref2, l_ref2 = run_oracle(good)
     assert_close(o2, l2, o_ref2, l_ref2)
+
+
+@pytest.mark.parametrize("kv", [BF16, FP8])
+def test_wait_timeout_is_reported_not_hung(kv):
+    """The device timeout path, made to run without any fault or hang: a plan whose
+    test-only option makes the first work unit never issue the copy of its page 2 and
+    shortens every bounded wait to ~2 ms. The warps that wait for that page give up, the
+    unit stops (in-flight copies drained, MMAs retired, tensor memory freed), the call
+    reports MLA_DEVICE_WAIT_TIMEOUT, and the next call on the same context is exact."""
+    from mla_speculative_verify_gb300.binding import MLA_DEVICE_WAIT_TIMEOUT
+
+    prob = inputs.make_problem(12, [64 * 40 + 7], [4], kv, seed=2980)
+    out, lse, st = run_gpu(prob, PlanOptions(force_splits=4, debug_skip_copy=3), check_status=False)
+    assert st & MLA_DEVICE_WAIT_TIMEOUT
+    o2, l2, st2 = run_gpu(prob)
+    assert st2 == 0
+    o_ref, l_ref = run_oracle(prob)
+    assert_close(o2, l2, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("H,q,ctx,kv", [(96, 64, 3000, BF16), (12, 512, 4000, FP8), (12, 2048, 3100, BF16)])
+def test_long_q_prefill_reduced_ctx(H, q, ctx, kv):
+    """Long verify / prefill chunks through the same kernel: q in {64, 512, 2048} tokens
+    (fold F = largest divisor of q with H F <= 128: 1 for H = 96, 8 for H = 12), every
+    token with its own causal key range (the earliest of the 2048 sees ctx - 2047 keys),
+    whole call against the oracle."""
+    _check(inputs.make_problem(H, [ctx], [q], kv, seed=3100 + q, poison_tail=True))

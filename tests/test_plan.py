@@ -78,8 +78,14 @@ def test_plan_invariants(seq_lens, q_lens, H, num_sms):
     assert covered == hd["n_part_rows"]
     for m in p["merges"]:
         assert m["n_splits"] >= 2
+    # bf16 partial O rows (1 KB each) and fp32 partial LSE, each block 256-byte aligned
     assert ws == (0 if hd["n_part_rows"] == 0 else
-                  ((hd["n_part_rows"] * 512 * 4 + 255) // 256 * 256 + (hd["n_part_rows"] * 4 + 255) // 256 * 256))
+                  ((hd["n_part_rows"] * 512 * 2 + 255) // 256 * 256 + (hd["n_part_rows"] * 4 + 255) // 256 * 256))
+    # the read-once flag: set exactly when the request is one fold group of one row tile
+    for u in p["units"]:
+        F = p["requests"][u["b"]]["fold"]
+        one_tile = q_lens[u["b"]] == F and H * F <= 48
+        assert u["flags"] == (1 if one_tile else 0)
     # the units fill the SMs without leaving most of them idle
     total_pages = sum(-(-s // 64) for s in seq_lens)
     if total_pages >= 4 * num_sms:
@@ -202,3 +208,12 @@ def test_plan_balances_ragged_batches(H):
     pages = [-(-(u["kv_end"] - u["kv_begin"]) // 64) for u in units]
     assert pages == sorted(pages, reverse=True)
     assert _lpt_makespan(pages, 152) <= 1.15 * (sum(pages) / 152 + 2)
+
+
+def test_plan_carries_the_timeout_test_option_only_when_asked():
+    buf, _ = binding.plan([4096], [2], 12, KV, 152)
+    assert read_plan(buf)["header"]["debug_skip_copy"] == 0
+    buf, _ = binding.plan([4096], [2], 12, KV, 152, binding.PlanOptions(debug_skip_copy=3))
+    assert read_plan(buf)["header"]["debug_skip_copy"] == 3
+    with pytest.raises(binding.MlaError):
+        binding.plan([4096], [2], 12, KV, 152, binding.PlanOptions(debug_skip_copy=-1))
