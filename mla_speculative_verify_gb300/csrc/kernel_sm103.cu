@@ -1070,16 +1070,20 @@ __global__ void __launch_bounds__(32 * W, 1024 / (32 * W)) lse_merge_kernel(cons
   acc_s[warp][lane] = acc;
   __syncthreads();
   if (warp == 0) {
-    float M = m_s[0];
+    // lane i < W holds warp i's (M_i, l_i): maximum and weights across the lanes
+    const float mi = lane < W ? m_s[lane] : -INFINITY;
+    float M = mi;
 #pragma unroll
-    for (int i = 1; i < W; ++i) M = fmaxf(M, m_s[i]);
-    float l = 0.f;
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float fi = mi == -INFINITY ? 0.f : __expf(mi - M);
+    float l = lane < W ? fi * l_s[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < W; ++i) {
-      const float f = m_s[i] == -INFINITY ? 0.f : __expf(m_s[i] - M);
+      const float f = __shfl_sync(0xffffffffu, fi, i);
       const float4 a = acc_s[i][lane];
-      l += f * l_s[i];
       r.x += f * a.x; r.y += f * a.y; r.z += f * a.z; r.w += f * a.w;
     }
     const float inv = 1.f / l;
