@@ -79,6 +79,8 @@ typedef struct {
   int min_pages_per_split; /* > 0: lower bound on pages per split unit */
   int force_fold;          /* > 0: use this fold factor F instead of the largest divisor rule
                               (must divide every q_len; F = 1 is the fold-less diagnostic mode) */
+  int unit_pages;          /* > 0: cut every fold group's key range into pieces of this many pages
+                              (the last one shorter) instead of the length the planner picks */
   int debug_skip_copy;     /* test of the device timeout path only, 0 in production: > 0 makes
                               the first work unit skip the copy of its page number
                               debug_skip_copy - 1 and shortens every bounded wait of the call to

@@ -36,7 +36,7 @@ _IP = ctypes.POINTER(ctypes.c_int)
 class PlanOptions(ctypes.Structure):
     _fields_ = [("force_splits", ctypes.c_int), ("max_rows_per_cta", ctypes.c_int),
                 ("min_pages_per_split", ctypes.c_int), ("force_fold", ctypes.c_int),
-                ("debug_skip_copy", ctypes.c_int)]
+                ("unit_pages", ctypes.c_int), ("debug_skip_copy", ctypes.c_int)]
 
 
 class MlaError(RuntimeError):

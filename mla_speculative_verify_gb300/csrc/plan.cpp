@@ -70,8 +70,10 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
                        o.max_rows_per_cta);
     cap = o.max_rows_per_cta;
   }
-  if (o.force_splits < 0 || o.min_pages_per_split < 0 || o.force_fold < 0 || o.debug_skip_copy < 0)
+  if (o.force_splits < 0 || o.min_pages_per_split < 0 || o.force_fold < 0 || o.unit_pages < 0 || o.debug_skip_copy < 0)
     return set_error(MLA_ERR_INVALID_ARG, "plan options must be >= 0");
+  if (o.force_splits > 0 && o.unit_pages > 0)
+    return set_error(MLA_ERR_INVALID_ARG, "force_splits and unit_pages exclude each other");
 
   long long total_q = 0;
   int max_pages = 0;
@@ -127,14 +129,21 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
   // Each group is cut into pieces of T pages (the last one shorter); all row tiles of the
   // group are cut at the same boundaries. The units are ordered longest first (below), so
   // the full-length units fill the SMs and the short tails run back to back on the SMs
-  // left over. T is the per-SM share of the tile-pages divided by k, for the k in 1..4
-  // whose schedule ends first in a model of the hardware's in-order CTA dispatch (each
-  // CTA also pays a start-up cost of about kStartPages pages); one long request keeps
-  // k = 1, ragged batches whose tiles do not divide evenly over the SMs pick a larger k.
-  // A split keeps at least min_pages pages.
+  // left over. T is the per-SM share of the tile-pages divided by k, for the k whose
+  // schedule ends first in a model of the hardware's in-order CTA dispatch: a unit costs
+  // a start-up of kStart page-times (its prologue, first copies and Q preparation, the
+  // epilogue and its split partial) plus its pages, each weighted by its row tile's cost
+  // (a tile of <= 32 rows of an e4m3 cache takes less than a 48-row tile). The model's
+  // constants were fitted to measured call times over forced piece lengths on GB300
+  // (bf16: a unit start ~ 6 page-times; e4m3: ~ 16). It sees each request's q, so a batch
+  // of ragged query lengths, whose fold groups differ in tile count, gets other piece
+  // lengths than a uniform one of the same total work. A split keeps at least min_pages
+  // pages.
   const int min_pages = o.min_pages_per_split > 0 ? o.min_pages_per_split : 4;
   const int max_splits = max_splits_for_merge();
-  constexpr long long kStartPages = 2;
+  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  const double start_cost = fp8 ? 16.0 : 6.0;
+  auto row_cost = [&](int nrows) { return (fp8 && nrows <= 32) ? 0.9 : 1.0; };
   long long tile_pages = 0;
   for (const Group& g : groups) tile_pages += (long long)(g.t1 - g.t0) * g.pages;
   auto assign = [&](long long T) {
@@ -150,26 +159,45 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
     return (int)((long long)g.pages * (s + 1) / g.n_split - (long long)g.pages * s / g.n_split);
   };
   long long best_T = std::max<long long>(min_pages, (tile_pages + num_sms - 1) / num_sms);
-  if (o.force_splits <= 0) {
-    long long best_end = -1;
-    std::vector<long long> lens;
-    for (int k = 1; k <= 4; ++k) {
-      const long long T = std::max<long long>(min_pages, (tile_pages + (long long)num_sms * k - 1) / ((long long)num_sms * k));
+  if (o.unit_pages > 0) best_T = o.unit_pages;
+  if (o.force_splits <= 0 && o.unit_pages <= 0) {
+    double best_end = -1;
+    std::vector<std::pair<int, double>> lens;  // (pages, per-page cost) of every unit
+    // candidates: the per-SM share divided by 1, 1.25, ... 8, and the longest group's
+    // pages divided into 1 .. 64 equal pieces
+    std::vector<long long> cands;
+    for (int k4 : {4, 5, 6, 8, 10, 12, 16, 20, 24, 32})
+      cands.push_back((4 * tile_pages + (long long)num_sms * k4 - 1) / ((long long)num_sms * k4));
+    int longest = 0;
+    for (const Group& g : groups) longest = std::max(longest, g.pages);
+    for (int n = 1; n <= 64; ++n) cands.push_back((longest + n - 1) / n);
+    std::sort(cands.begin(), cands.end());
+    cands.erase(std::unique(cands.begin(), cands.end()), cands.end());
+    for (long long c : cands) {
+      const long long T = std::max<long long>(min_pages, c);
+      // more than 16 waves of units (beyond one unit per row tile) never pays for its
+      // start-up costs; skipping those keeps the search cheap for very long batches
+      long long n_units = 0;
+      for (const Group& g : groups) n_units += (long long)(g.t1 - g.t0) * ((g.pages + T - 1) / T);
+      if (n_units > std::max<long long>(16LL * num_sms, (long long)tiles.size()) && !cands.empty() && c != cands.back())
+        continue;
       assign(T);
       lens.clear();
       for (const Group& g : groups)
-        for (int s = 0; s < g.n_split; ++s) lens.insert(lens.end(), g.t1 - g.t0, piece_pages(g, s));
-      std::sort(lens.begin(), lens.end(), std::greater<long long>());
-      std::priority_queue<long long, std::vector<long long>, std::greater<long long>> sm;
-      for (int i = 0; i < num_sms; ++i) sm.push(0);
-      long long end = 0;
-      for (long long L : lens) {
-        const long long t = sm.top() + L + kStartPages;
+        for (int s = 0; s < g.n_split; ++s)
+          for (size_t t = g.t0; t < g.t1; ++t) lens.emplace_back(piece_pages(g, s), row_cost(tiles[t].nrows));
+      std::stable_sort(lens.begin(), lens.end(),
+                       [](const std::pair<int, double>& a, const std::pair<int, double>& b) { return a.first > b.first; });
+      std::priority_queue<double, std::vector<double>, std::greater<double>> sm;
+      for (int i = 0; i < num_sms; ++i) sm.push(0.0);
+      double end = 0;
+      for (const auto& L : lens) {
+        const double t = sm.top() + start_cost + L.first * L.second;
         sm.pop();
         sm.push(t);
         end = std::max(end, t);
       }
-      if (best_end < 0 || end < best_end) {
+      if (best_end < 0 || end < best_end - 1e-9) {
         best_end = end;
         best_T = T;
       }

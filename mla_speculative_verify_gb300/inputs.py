@@ -173,16 +173,24 @@ def workload_h96(q: int, ctx: int, kv_dtype: str, seed: int = 1004) -> Problem:
     return make_problem(96, [ctx], [q], kv_dtype, seed, name=f"h96_q{q}_ctx{ctx}_{kv_dtype}")
 
 
-def workload_ragged(H: int, pattern: str = "ragged", B: int = 32, ctx_lo: int = 16384,
-                    ctx_hi: int = 32768, seed: int = 1005) -> Problem:
-    """B=32 batch, H in {48,128}, q from {1,2,3,4} (seeded MTP-3 pattern) or uniform 4,
-    ctx ~ U[ctx_lo, ctx_hi], fp8 e4m3, shuffled global page pool."""
-    g = np.random.default_rng(seed)
+def ragged_lengths(pattern: str = "ragged", B: int = 32, ctx_lo: int = 16384, ctx_hi: int = 32768,
+                   seed: int = 1005):
+    """(seq_lens, q_lens) of the B=32 batch: ctx ~ U[ctx_lo, ctx_hi]; q from {1,2,3,4}
+    (seeded MTP-3 pattern) or uniform 4. Both patterns share the context lengths (the same
+    geometry, only q differs)."""
+    seq_lens = np.random.default_rng(seed).integers(ctx_lo, ctx_hi + 1, size=B)
     if pattern == "ragged":
-        q_lens = g.integers(1, 5, size=B)
+        q_lens = np.random.default_rng(seed + 1).integers(1, 5, size=B)
     elif pattern == "uniform":
         q_lens = np.full(B, 4)
     else:
         raise ValueError(pattern)
-    seq_lens = g.integers(ctx_lo, ctx_hi + 1, size=B)
+    return seq_lens, q_lens
+
+
+def workload_ragged(H: int, pattern: str = "ragged", B: int = 32, ctx_lo: int = 16384,
+                    ctx_hi: int = 32768, seed: int = 1005) -> Problem:
+    """B=32 batch, H in {48,128}, the lengths of ragged_lengths, fp8 e4m3, shuffled global
+    page pool."""
+    seq_lens, q_lens = ragged_lengths(pattern, B, ctx_lo, ctx_hi, seed)
     return make_problem(H, seq_lens, q_lens, KV_FP8, seed, name=f"h{H}_b{B}_{pattern}_fp8")

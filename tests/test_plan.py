@@ -6,7 +6,7 @@ import ctypes
 import numpy as np
 import pytest
 
-from mla_speculative_verify_gb300 import binding
+from mla_speculative_verify_gb300 import binding, inputs
 from tests.plan_reader import read_plan
 
 KV = binding.MLA_KV_BF16
@@ -217,3 +217,48 @@ def test_plan_carries_the_timeout_test_option_only_when_asked():
     assert read_plan(buf)["header"]["debug_skip_copy"] == 3
     with pytest.raises(binding.MlaError):
         binding.plan([4096], [2], 12, KV, 152, binding.PlanOptions(debug_skip_copy=-1))
+
+
+def _max_piece(plan_buf):
+    return max(-(-(u["kv_end"] - u["kv_begin"]) // 64) for u in read_plan(plan_buf)["units"])
+
+
+@pytest.mark.parametrize("H,pattern,best", [(48, "ragged", 212), (48, "uniform", 342), (128, "ragged", 318),
+                                            (128, "uniform", 342)])
+def test_planner_picks_the_piece_length_measured_fastest(H, pattern, best):
+    """The B=32 MTP-3 batches (e4m3, ctx 16k-32k, both patterns on the same context lengths).
+    On GB300 every piece length the planner can choose was timed (mla_decode_run, graph
+    replay); the fastest were 212 / 342 pages (H=48 ragged 279.0 us, uniform 434.2 us) and
+    318 / 342 pages (H=128 ragged 742.6 us, uniform 1164.7 us), against 290.1 / 436.9 /
+    762.8 / 1193.7 us for the earlier start-up cost of 2 page-times. The planner's dispatch
+    model must keep choosing those lengths."""
+    seq_lens, q_lens = inputs.ragged_lengths(pattern)
+    buf, _ = binding.plan(seq_lens, q_lens, H, binding.MLA_KV_FP8_E4M3, 152)
+    assert _max_piece(buf) == best
+
+
+def test_ragged_and_uniform_batches_of_equal_work_get_different_pieces():
+    """flashinfer #5588 ("What was measured", host-plan row) found that unit sizes good for
+    ragged query lengths lose on uniform ones of the same geometry, and that a plan built
+    from host scalars alone could not tell the two apart. This planner receives every
+    request's q: a ragged (MTP-3) and a uniform (q = 4) H=128 batch of the same total
+    tile-pages (the uniform batch's contexts scaled down) get different piece lengths and
+    unit counts, because their row tiles (48- and 32-row) fall into fold groups differently."""
+    sl_r, ql_r = inputs.ragged_lengths("ragged")
+    sl_u, ql_u = inputs.ragged_lengths("uniform")
+    sl_u = np.maximum(64, (sl_u * (ql_r.sum() / ql_u.sum())).astype(np.int64))
+    kv = binding.MLA_KV_FP8_E4M3
+    br, _ = binding.plan(sl_r, ql_r, 128, kv, 152)
+    bu, _ = binding.plan(sl_u, ql_u, 128, kv, 152)
+    work = [sum(-(-(x["kv_end"] - x["kv_begin"]) // 64) for x in read_plan(b)["units"]) for b in (br, bu)]
+    assert abs(work[0] - work[1]) <= 0.02 * work[0]
+    assert _max_piece(br) != _max_piece(bu)
+    assert len(read_plan(br)["units"]) != len(read_plan(bu)["units"])
+
+
+def test_unit_pages_option_forces_the_piece_length():
+    buf, _ = binding.plan([131072], [1], 12, KV, 152, binding.PlanOptions(unit_pages=20))
+    pages = sorted({-(-(u["kv_end"] - u["kv_begin"]) // 64) for u in read_plan(buf)["units"]})
+    assert pages == [8, 20]  # 2048 pages = 102 x 20 + 8
+    with pytest.raises(binding.MlaError):
+        binding.plan([4096], [2], 12, KV, 152, binding.PlanOptions(unit_pages=8, force_splits=2))
