@@ -460,7 +460,7 @@ def main():
                          hbm_frac=round(hf, 3), hbm_frac_rated=round(gbs / HBM_RATED_GBS, 3),
                          tensor_frac=round(tf, 3), combined_frac=round(max(hf, tf), 3),
                          traffic=traffic.get(prob.name), units=c["dec"].info["n_units"],
-                         merge_items=c["dec"].info["n_merge"]))
+                         cta_pair=c["dec"].cta_pair, merge_items=c["dec"].info["n_merge"]))
     # roofline of the dominant kernel (the fold kernel, launched once per call; each timed
     # call is the whole mla_decode_run, fold + merge): the step's algorithmic bytes (or
     # flops, when the step's tensor time at peak exceeds its HBM time) over the step's call
@@ -501,8 +501,9 @@ def main():
                                       "from the committed profile when the hash of the kernel sources matches, "
                                       "else null"),
                      "algorithmic_bytes": dbytes, "algorithmic_flops": dflops,
-                     "kernel": "fold_decode_kernel + lse_merge_kernel, per mla_decode_run call, mean over "
-                               f"the step's {n_calls} calls",
+                     "kernel": ("fold kernel (fold_decode_kernel on single CTAs, or fold_pair_kernel on clusters "
+                                "of two CTAs for 49..96-row bf16 fold groups) + lse_merge_kernel, per "
+                                f"mla_decode_run call, mean over the step's {n_calls} calls"),
                      "peak_source": (f"{peak_src} bf16_tflops for bf16 calls, x 2 (nominal ratio) for e4m3 calls"
                                      if tensor_bound else f"{peak_src} hbm_gbs"),
                      **({} if tensor_bound else {"peak_rated": HBM_RATED_GBS,

@@ -81,6 +81,11 @@ typedef struct {
                               (must divide every q_len; F = 1 is the fold-less diagnostic mode) */
   int unit_pages;          /* > 0: cut every fold group's key range into pieces of this many pages
                               (the last one shorter) instead of the length the planner picks */
+  int cta_pair;            /* > 0: with a bf16 cache whose fold groups all have 49..96 rows,
+                              run each group on a cluster of two CTAs that split the page
+                              columns (0: <= 48-row single-CTA tiles) */
+  int pair_slots;          /* > 0: clusters of two CTAs the device runs at once (the planner's
+                              dispatch model); 0: num_sms / 2 */
   int debug_skip_copy;     /* test of the device timeout path only, 0 in production: > 0 makes
                               the first work unit skip the copy of its page number
                               debug_skip_copy - 1 and shortens every bounded wait of the call to
@@ -183,6 +188,16 @@ int mla_decode_run_static_ws(const void* plan_dev, const void* plan_host, size_t
                              const void* kv_cache, const int32_t* page_table, int page_table_stride, int num_pages,
                              const int32_t* seq_lens, const int32_t* q_lens, float sm_scale, float kv_scale, void* out,
                              float* lse, int32_t* status_dev, void* stream);
+
+/*
+ * mla_device_pair_slots -- how many clusters of two CTAs of the two-CTA decode kernel the
+ * device runs at once (cudaOccupancyMaxActiveClusters). A plan for fold groups of 49..96
+ * rows with a bf16 cache runs on such clusters; pass this number as
+ * mla_plan_options.pair_slots so that the planner's dispatch model matches the device
+ * (a GPC with an odd number of free SMs leaves one SM out). Sets the current device to
+ * `device` for the query and restores it.
+ */
+int mla_device_pair_slots(int device, int* slots);
 
 /* Message of the last failed call on this thread ("" if none). */
 const char* mla_last_error(void);

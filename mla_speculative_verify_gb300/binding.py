@@ -36,7 +36,8 @@ _IP = ctypes.POINTER(ctypes.c_int)
 class PlanOptions(ctypes.Structure):
     _fields_ = [("force_splits", ctypes.c_int), ("max_rows_per_cta", ctypes.c_int),
                 ("min_pages_per_split", ctypes.c_int), ("force_fold", ctypes.c_int),
-                ("unit_pages", ctypes.c_int), ("debug_skip_copy", ctypes.c_int)]
+                ("unit_pages", ctypes.c_int), ("cta_pair", ctypes.c_int), ("pair_slots", ctypes.c_int),
+                ("debug_skip_copy", ctypes.c_int)]
 
 
 class MlaError(RuntimeError):
@@ -57,6 +58,7 @@ SIGNATURES = {
                                       ctypes.c_float, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "mla_decode_run_static_ws": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P, _P, _P, ctypes.c_int, ctypes.c_int, _P,
                                                  _P, ctypes.c_float, ctypes.c_float, _P, _P, _P, _P]),
+    "mla_device_pair_slots": (ctypes.c_int, [ctypes.c_int, _IP]),
     "mla_last_error": (ctypes.c_char_p, []),
     "mla_version": (ctypes.c_int, []),
 }
@@ -121,6 +123,19 @@ def plan(seq_lens, q_lens, num_heads: int, kv_dtype: int, num_sms: int, options:
                                 ctypes.byref(ws))
     check(rc, lib)
     return buf, int(ws.value)
+
+
+_pair_slots = {}
+
+
+def device_pair_slots(device: int) -> int:
+    """mla_device_pair_slots: clusters of two CTAs the device runs at once (cached)."""
+    if device not in _pair_slots:
+        lib = load()
+        n = ctypes.c_int(0)
+        check(lib.mla_device_pair_slots(int(device), ctypes.byref(n)), lib)
+        _pair_slots[device] = int(n.value)
+    return _pair_slots[device]
 
 
 def plan_info(plan_bytes: np.ndarray) -> dict:

@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(HERE, "_lib")
 LIB_NAME = "libmla_verify_sm103.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 
-CUDA_SOURCES = ["kernel_sm103.cu", "static_workspace.cu"]
+CUDA_SOURCES = ["kernel_sm103.cu", "kernel_pair_sm103.cu", "static_workspace.cu"]
 HOST_SOURCES = ["plan.cpp", "status.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

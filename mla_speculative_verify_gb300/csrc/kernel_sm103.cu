@@ -69,6 +69,7 @@
 
 #include "mla_decode.h"
 #include "plan_format.h"
+#include "decode_common.cuh"
 #include "ptx.cuh"
 #include "status.h"
 
@@ -109,8 +110,6 @@ struct Geo {
 };
 
 
-constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, each owning half of the columns
-constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 // Warps: producer, MMA warps, softmax. Every accumulator is written by one thread in
 // program order, so a unit's result is the same bit for bit on every run.
 //   bf16:  three S^T warps, each a third of the K-steps into a partial accumulator of its
@@ -140,28 +139,6 @@ constexpr float kRefSlack = 8.0f;    // octaves a score may exceed the row refer
 // already P times 2^4; l carries the same factor, which cancels in O / l and in the LSE.
 constexpr float kRefSlackFp8 = 4.0f;
 constexpr float kPShiftFp8 = 4.0f;
-constexpr long long kWaitBudget = 2000000000LL;  // cycles (~1 s) before a wait gives up
-constexpr long long kWaitBudgetTest = 4000000LL; // ~2 ms: the budget of a call that tests the timeout path
-
-struct Params {
-  const PlanUnit* units;   // the plan's unit table (one record per CTA)
-  const __nv_bfloat16* q;  // the e4m3 path converts its Q tile from global memory
-  int q_rows;              // rows of q (sum q_lens * H)
-  const int32_t* page_table;
-  int pt_stride, num_pages, H;
-  const int32_t* seq_lens;
-  const int32_t* q_lens;
-  float score_scale_log2;  // sm_scale * kv_scale * log2(e)
-  float out_scale;         // kv_scale (1 for a bf16 cache)
-  __nv_bfloat16* out;
-  float* lse;
-  __nv_bfloat16* part_o;  // split partials of O (bf16, each normalised by its split's l)
-  float* part_lse;
-  int32_t* status;
-  long long wait_budget;  // cycles a bounded wait may take (kWaitBudget; kWaitBudgetTest in a timeout test)
-  int skip_copy;          // page of the first unit whose copy is never issued (timeout test), or -1
-};
-
 struct Misc {
   uint64_t bar_q;
   uint64_t kv_full[4], kv_empty[4];
@@ -180,56 +157,6 @@ struct Misc {
 };
 static_assert(offsetof(Misc, ref) % 16 == 0, "float4 reads of ref need 16-byte alignment");
 static_assert(sizeof(Misc) <= kMiscBytes, "misc block too small");
-
-__device__ __forceinline__ void report(int32_t* status, int bits) {
-  if (status) atomicOr(status, bits);
-}
-
-// Bounded wait: false when the budget ran out or another warp aborted the unit.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort, const Params& p) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  long long t0 = clock64();
-  while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (clock64() - t0 > p.wait_budget) {
-      *abort = 1;
-      report(p.status, MLA_DEVICE_WAIT_TIMEOUT);
-      return false;
-    }
-  }
-}
-
-// Warp-uniform bounded wait: lane 0 polls, the result is broadcast to the warp.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, const Params& p) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort, p) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// Barriers among the softmax warps only (named barrier 1). Every softmax warp reaches
-// every one of them the same number of times, whatever happens to the unit: decisions
-// that end the loop are taken from a barrier's OR-reduction, so all warps take them
-// together.
-constexpr uint32_t kSoftmaxBar = 1;
-__device__ __forceinline__ void softmax_sync() { ptx::bar_sync(kSoftmaxBar, kSoftmaxThreads); }
-__device__ __forceinline__ bool softmax_any(bool pred) { return ptx::bar_red_or(kSoftmaxBar, kSoftmaxThreads, pred); }
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float lg2(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 
 // An fp32 rounded to the precision of e4m3 (4 significant bits, round to nearest even),
 // still as fp32; exact for magnitudes in e4m3's normal range.
@@ -288,14 +215,6 @@ __device__ __forceinline__ void issue_ot_mma_e4m3(uint32_t tmem, uint32_t skv, u
   const uint64_t ad = ptx::smem_desc(v0 + 2048 * k, G::kChunkBytes, 512, ptx::kSwizzle64B);
   const uint64_t bd = ptx::smem_desc(pt0 + part * (kTileKeys * 64) + 2048 * k, 4096, 512, ptx::kSwizzle64B);
   ptx::mma_e4m3_ss(tmem + kTmemO + 64 * blk, ad, bd, idesc_o, 1u);
-}
-
-// Waits (bounded) until the tcgen05 operations this lane issued have completed.
-__device__ __forceinline__ void drain_mmas(uint64_t* done, long long budget) {
-  ptx::mma_commit(done);
-  long long t0c = clock64();
-  while (!ptx::mbar_try_wait(done, 0) && clock64() - t0c < budget) {
-  }
 }
 
 struct SoftmaxArgs {
@@ -1151,8 +1070,11 @@ int max_splits_for_merge() { return kMergeMaxSplits; }
 // ------------------------------------------------------------------ host side
 size_t workspace_bytes_for(int n_part_rows);
 int check_plan(const void* plan_host, size_t plan_bytes, const PlanHeader** out);
+int launch_pair_kernel(int dev, const PlanHeader* h, const void* q, const void* kv_cache, int num_pages,
+                       const Params& prm, cudaStream_t st);
+int pair_slots_on_device(int dev, int* slots);
 
-static PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -1249,7 +1171,7 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
   if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
   rc = prepare_device(dev);
   if (rc != MLA_OK) return rc;
-  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encoder();
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return set_error(MLA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
 
   const bool fp8 = h->kv_dtype == MLA_KV_FP8_E4M3;
@@ -1281,12 +1203,18 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
   prm.wait_budget = h->debug_skip_copy > 0 ? kWaitBudgetTest : kWaitBudget;
   prm.skip_copy = h->debug_skip_copy - 1;
   cudaStream_t st = (cudaStream_t)stream;
-  if (fp8)
-    fold_decode_kernel<true><<<h->n_units, Roles<true>::kThreads, kSmemBytes, st>>>(tq, tkv, prm);
-  else
-    fold_decode_kernel<false><<<h->n_units, Roles<false>::kThreads, kSmemBytes, st>>>(tq, tkv, prm);
-  ce = cudaGetLastError();
-  if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "fold kernel launch: %s", cudaGetErrorString(ce));
+  if (h->cta_pair) {
+    if (fp8) return set_error(MLA_ERR_PLAN, "a two-CTA plan needs a bf16 cache");
+    rc = launch_pair_kernel(dev, h, q, kv_cache, num_pages, prm, st);
+    if (rc != MLA_OK) return rc;
+  } else {
+    if (fp8)
+      fold_decode_kernel<true><<<h->n_units, Roles<true>::kThreads, kSmemBytes, st>>>(tq, tkv, prm);
+    else
+      fold_decode_kernel<false><<<h->n_units, Roles<false>::kThreads, kSmemBytes, st>>>(tq, tkv, prm);
+    ce = cudaGetLastError();
+    if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "fold kernel launch: %s", cudaGetErrorString(ce));
+  }
   if (h->n_merge > 0) {
     // the warp-per-row merge when every row tile has few splits, else the CTA-per-row one
     const PlanMerge* mh = (const PlanMerge*)((const uint8_t*)plan_host + h->merge_off);
@@ -1316,4 +1244,19 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
     if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "merge kernel launch: %s", cudaGetErrorString(ce));
   }
   return MLA_OK;
+}
+
+extern "C" int mla_device_pair_slots(int device, int* slots) {
+  clear_error();
+  if (!slots) return set_error(MLA_ERR_INVALID_ARG, "slots must not be NULL");
+  int rc = prepare_device(device);
+  if (rc != MLA_OK) return rc;
+  int cur = 0;
+  cudaError_t ce = cudaGetDevice(&cur);
+  if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
+  if (cur != device && (ce = cudaSetDevice(device)) != cudaSuccess)
+    return set_error(MLA_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(ce));
+  rc = pair_slots_on_device(device, slots);
+  if (cur != device) cudaSetDevice(cur);
+  return rc;
 }

@@ -29,6 +29,7 @@ namespace mla {
 
 int rows_cap_for(int kv_dtype);  // defined next to the kernel
 int max_splits_for_merge();       // defined next to the merge kernel
+int pair_rows_cap();              // defined next to the two-CTA kernel
 
 static int fold_factor(int q, int H) {
   int best = 1;
@@ -70,7 +71,8 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
                        o.max_rows_per_cta);
     cap = o.max_rows_per_cta;
   }
-  if (o.force_splits < 0 || o.min_pages_per_split < 0 || o.force_fold < 0 || o.unit_pages < 0 || o.debug_skip_copy < 0)
+  if (o.force_splits < 0 || o.min_pages_per_split < 0 || o.force_fold < 0 || o.unit_pages < 0 || o.cta_pair < 0 ||
+      o.pair_slots < 0 || o.debug_skip_copy < 0)
     return set_error(MLA_ERR_INVALID_ARG, "plan options must be >= 0");
   if (o.force_splits > 0 && o.unit_pages > 0)
     return set_error(MLA_ERR_INVALID_ARG, "force_splits and unit_pages exclude each other");
@@ -87,6 +89,19 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
     max_pages = std::max(max_pages, (ctx + kPage - 1) / kPage);
   }
   if (total_q * num_heads > (1LL << 30)) return set_error(MLA_ERR_INVALID_ARG, "too many query rows");
+
+  // On request (cta_pair), a bf16 cache whose every fold group has 49..96 packed rows runs
+  // on clusters of two CTAs, one unit per fold group and key piece: each CTA streams half
+  // of every page's columns, so the page enters the pair once instead of once per 48-row
+  // tile. (Off by default: on GB300 the 48-row single-CTA tiles are faster.)
+  bool pair = kv_dtype == MLA_KV_BF16 && o.cta_pair > 0 && o.max_rows_per_cta == 0;
+  for (int b = 0; pair && b < batch; ++b) {
+    const int F = o.force_fold > 0 ? o.force_fold : fold_factor(q_lens_h[b], num_heads);
+    const int R = F * num_heads;
+    pair = R > cap && R <= pair_rows_cap();
+  }
+  if (pair) cap = pair_rows_cap();
+  const int slots = pair ? (o.pair_slots > 0 ? o.pair_slots : std::max(1, num_sms / 2)) : num_sms;
 
   // --- row tiles ----------------------------------------------------------------------
   struct RowTile { int b, qrow0, nrows, pages; };
@@ -158,7 +173,7 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
     if (g.cap > 0) return std::min(g.pages, (s + 1) * g.cap) - s * g.cap;
     return (int)((long long)g.pages * (s + 1) / g.n_split - (long long)g.pages * s / g.n_split);
   };
-  long long best_T = std::max<long long>(min_pages, (tile_pages + num_sms - 1) / num_sms);
+  long long best_T = std::max<long long>(min_pages, (tile_pages + slots - 1) / slots);
   if (o.unit_pages > 0) best_T = o.unit_pages;
   if (o.force_splits <= 0 && o.unit_pages <= 0) {
     double best_end = -1;
@@ -167,7 +182,7 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
     // pages divided into 1 .. 64 equal pieces
     std::vector<long long> cands;
     for (int k4 : {4, 5, 6, 8, 10, 12, 16, 20, 24, 32})
-      cands.push_back((4 * tile_pages + (long long)num_sms * k4 - 1) / ((long long)num_sms * k4));
+      cands.push_back((4 * tile_pages + (long long)slots * k4 - 1) / ((long long)slots * k4));
     int longest = 0;
     for (const Group& g : groups) longest = std::max(longest, g.pages);
     for (int n = 1; n <= 64; ++n) cands.push_back((longest + n - 1) / n);
@@ -179,7 +194,7 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
       // start-up costs; skipping those keeps the search cheap for very long batches
       long long n_units = 0;
       for (const Group& g : groups) n_units += (long long)(g.t1 - g.t0) * ((g.pages + T - 1) / T);
-      if (n_units > std::max<long long>(16LL * num_sms, (long long)tiles.size()) && !cands.empty() && c != cands.back())
+      if (n_units > std::max<long long>(16LL * slots, (long long)tiles.size()) && !cands.empty() && c != cands.back())
         continue;
       assign(T);
       lens.clear();
@@ -189,7 +204,7 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
       std::stable_sort(lens.begin(), lens.end(),
                        [](const std::pair<int, double>& a, const std::pair<int, double>& b) { return a.first > b.first; });
       std::priority_queue<double, std::vector<double>, std::greater<double>> sm;
-      for (int i = 0; i < num_sms; ++i) sm.push(0.0);
+      for (int i = 0; i < slots; ++i) sm.push(0.0);
       double end = 0;
       for (const auto& L : lens) {
         const double t = sm.top() + start_cost + L.first * L.second;
@@ -243,7 +258,7 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
   }
   // Longest units first: when the grid needs more than one wave, the SMs that finish
   // early pick up the short units. (Stable, so the tiles of a group stay adjacent.)
-  if ((long long)units.size() > num_sms)
+  if ((long long)units.size() > slots)
     std::stable_sort(units.begin(), units.end(), [](const PlanUnit& a, const PlanUnit& c) {
       return a.kv_end - a.kv_begin > c.kv_end - c.kv_begin;
     });
@@ -270,6 +285,7 @@ extern "C" int mla_decode_plan_ex(const int32_t* seq_lens_h, const int32_t* q_le
   h.req_off = (int32_t)req_off; h.units_off = (int32_t)units_off; h.merge_off = (int32_t)merge_off;
   h.total_bytes = (int32_t)total;
   h.debug_skip_copy = o.debug_skip_copy;
+  h.cta_pair = pair ? 1 : 0;
   memcpy(base, &h, sizeof h);
   memcpy(base + req_off, reqs.data(), sizeof(PlanRequest) * batch);
   if (!units.empty()) memcpy(base + units_off, units.data(), sizeof(PlanUnit) * units.size());

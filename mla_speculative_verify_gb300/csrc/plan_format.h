@@ -8,7 +8,7 @@
 namespace mla {
 
 constexpr uint32_t kPlanMagic = 0x564C4D41u;  // "AMLV"
-constexpr uint32_t kPlanVersion = 4;
+constexpr uint32_t kPlanVersion = 5;
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kPage = 64;
@@ -29,15 +29,18 @@ struct PlanHeader {
   int32_t req_off, units_off, merge_off;  // byte offsets from the plan start
   int32_t total_bytes;
   int32_t debug_skip_copy;  // mla_plan_options.debug_skip_copy (0 in production plans)
+  int32_t cta_pair;         // 1: every unit is one fold group of 49..96 rows for a cluster of two CTAs
+  int32_t reserved[3];
 };
-static_assert(sizeof(PlanHeader) == 64, "plan header is 64 bytes");
+static_assert(sizeof(PlanHeader) == 80, "plan header is 80 bytes");
 
 // One request: ctx keys (verify tokens included), q verify tokens, first global token.
 struct PlanRequest {
   int32_t ctx, q, tok0, fold;
 };
 
-// One CTA work unit: a tile of packed rows of one fold group over one key range.
+// One work unit: a tile of packed rows of one fold group over one key range, for one CTA
+// (or, in a cta_pair plan, for a cluster of two CTAs that split the tile's columns).
 // Packed rows are global Q rows qrow0 .. qrow0 + nrows - 1 (row = token * H + head).
 struct PlanUnit {
   int32_t b;           // request

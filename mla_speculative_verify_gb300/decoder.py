@@ -38,9 +38,18 @@ class VerifyDecoder:
         if num_sms is None:
             num_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
         self.num_sms = int(num_sms)
+        if self.device.type == "cuda":
+            # clusters of two CTAs the device runs at once, for plans that use them
+            opts = binding.PlanOptions() if options is None else options
+            if opts.pair_slots == 0 and kv_dtype == "bf16":
+                opts = binding.PlanOptions.from_buffer_copy(opts)
+                opts.pair_slots = binding.device_pair_slots(self.device.index)
+            options = opts
         self.plan_host, self.workspace_bytes = binding.plan(self.seq_lens, self.q_lens, self.num_heads,
                                                             KV_DTYPES[kv_dtype], self.num_sms, options)
         self.info = binding.plan_info(self.plan_host)
+        # the plan runs on clusters of two CTAs (PlanHeader.cta_pair, the int32 at byte 64)
+        self.cta_pair = bool(int(self.plan_host[64:68].view(np.int32)[0]))
         self.plan_dev = torch.from_numpy(self.plan_host).to(self.device)
         self.workspace = (torch.empty(self.workspace_bytes, dtype=torch.uint8, device=self.device)
                           if self.workspace_bytes else None)

@@ -50,7 +50,7 @@ def test_plan_invariants(seq_lens, q_lens, H, num_sms):
         assert 0 <= u["kv_begin"] < u["kv_end"] <= ctx
         assert u["kv_begin"] % 64 == 0
         assert u["kv_end"] % 64 == 0 or u["kv_end"] == ctx
-        assert 1 <= u["nrows"] <= 48
+        assert 1 <= u["nrows"] <= (96 if hd["cta_pair"] else 48)
         # the request fields repeated in the unit record match the request table
         req = p["requests"][b]
         assert (u["ctx"], u["q"], u["tok0"]) == (req["ctx"], req["q"], req["tok0"]) == (ctx, q_lens[b], cu[b])
@@ -84,12 +84,14 @@ def test_plan_invariants(seq_lens, q_lens, H, num_sms):
     # the read-once flag: set exactly when the request is one fold group of one row tile
     for u in p["units"]:
         F = p["requests"][u["b"]]["fold"]
-        one_tile = q_lens[u["b"]] == F and H * F <= 48
+        one_tile = q_lens[u["b"]] == F and (H * F <= 48 or hd["cta_pair"])
         assert u["flags"] == (1 if one_tile else 0)
+    # clusters of two CTAs only on request
+    assert hd["cta_pair"] == 0
     # the units fill the SMs without leaving most of them idle
     total_pages = sum(-(-s // 64) for s in seq_lens)
     if total_pages >= 4 * num_sms:
-        assert len(p["units"]) >= num_sms // 2
+        assert len(p["units"]) * (2 if hd["cta_pair"] else 1) >= num_sms // 2
 
 
 def test_plan_forced_splits_and_fold():
@@ -190,10 +192,12 @@ def test_plan_single_long_request_fits_one_wave(q):
     """One long request: at most one unit per SM, and no unit much longer than the per-SM
     share of the tile-pages."""
     buf, _ = binding.plan([131072], [q], 12, KV, 152)
-    units = read_plan(buf)["units"]
-    assert len(units) <= 152
+    p = read_plan(buf)
+    units = p["units"]
+    slots = 76 if p["header"]["cta_pair"] else 152  # q = 8: 96-row groups on clusters of two CTAs
+    assert len(units) <= slots
     pages = [-(-(u["kv_end"] - u["kv_begin"]) // 64) for u in units]
-    assert max(pages) <= -(-sum(pages) // 152) + 1
+    assert max(pages) <= -(-sum(pages) // slots) + 1
 
 
 @pytest.mark.parametrize("H", [48, 96, 128])
@@ -262,3 +266,21 @@ def test_unit_pages_option_forces_the_piece_length():
     assert pages == [8, 20]  # 2048 pages = 102 x 20 + 8
     with pytest.raises(binding.MlaError):
         binding.plan([4096], [2], 12, KV, 152, binding.PlanOptions(unit_pages=8, force_splits=2))
+
+
+@pytest.mark.parametrize("seq_lens,q_lens,H", [([131072], [8], 12), ([3000, 5000], [8, 16], 12), ([700], [1], 80),
+                                               ([900], [6], 16), ([700], [4], 12), ([700], [1], 128)])
+def test_cta_pair_plans(seq_lens, q_lens, H):
+    """With cta_pair, a bf16 plan whose every fold group has 49..96 rows gets one unit per
+    fold group and key piece (rows up to 96), sized for num_sms / 2 clusters; other plans
+    (48 rows, 128 rows, an e4m3 cache) stay on single CTAs."""
+    rows = [_fold(q, H) * H for q in q_lens]
+    eligible = all(48 < r <= 96 for r in rows)
+    for kv in (KV, binding.MLA_KV_FP8_E4M3):
+        buf, _ = binding.plan(seq_lens, q_lens, H, kv, 152, binding.PlanOptions(cta_pair=1))
+        p = read_plan(buf)
+        assert p["header"]["cta_pair"] == int(eligible and kv == KV)
+        if p["header"]["cta_pair"]:
+            assert {u["nrows"] for u in p["units"]} == set(rows)
+            if len(seq_lens) == 1 and q_lens[0] * H == rows[0]:
+                assert len(p["units"]) <= 76
