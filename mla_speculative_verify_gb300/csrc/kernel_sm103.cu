@@ -330,8 +330,28 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
   int lim_min = a.kv_end;
   for (int n = 0; n < a.nrows; ++n) lim_min = min(lim_min, ms->lim[n]);
   float l_acc[NC];
+  // e4m3: this thread's copies of its rows' references (they change only when a row
+  // moves), so the shared-memory pipe, which the e4m3 path fills, serves fewer loads; the
+  // bf16 path reads them from shared memory (its registers are spoken for)
+  float rref[kFp8 ? NC : 1];
 #pragma unroll
   for (int i = 0; i < NC; ++i) l_acc[i] = 0.f;
+#pragma unroll
+  for (int i = 0; i < (kFp8 ? NC : 1); ++i) rref[i] = -INFINITY;
+  // e4m3: the rows' score scales (fixed for the unit; the barrier above published them)
+  float csr[kFp8 ? NC : 1];
+#pragma unroll
+  for (int i = 0; i < (kFp8 ? NC : 1); ++i)
+    csr[i] = kFp8 ? ms->colscale[16 * (i / 4) + col0 + (i % 4)] : 0.f;
+  auto ref4 = [&](int c, float* r) {
+    if constexpr (kFp8) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) r[j] = rref[4 * c + j];
+    } else {
+      const float4 rr = *reinterpret_cast<const float4*>(&ms->ref[16 * c + col0]);
+      r[0] = rr.x; r[1] = rr.y; r[2] = rr.z; r[3] = rr.w;
+    }
+  };
   const float scale = p.score_scale_log2;
   for (int t = 0; !stop && t < a.ntiles; ++t) {
     const int sb = t & 1;
@@ -377,11 +397,13 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         const int n0 = 16 * c + col0;
-        const float4 rr = *reinterpret_cast<const float4*>(&ms->ref[n0]);
-        float4 cs = make_float4(scale, scale, scale, scale);
-        if constexpr (kFp8) cs = *reinterpret_cast<const float4*>(&ms->colscale[n0]);
-        const float rrv[4] = {rr.x, rr.y, rr.z, rr.w};
-        const float csv[4] = {cs.x, cs.y, cs.z, cs.w};
+        float rrv[4];
+        ref4(c, rrv);
+        float csv[4] = {scale, scale, scale, scale};
+        if constexpr (kFp8) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) csv[j] = csr[4 * c + j];
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           float v = x[4 * c + j] * csv[j];
@@ -413,6 +435,10 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
       softmax_sync();
 #pragma unroll
       for (int i = 0; i < NC; ++i) l_acc[i] *= ms->alpha[16 * (i / 4) + col0 + (i % 4)];
+      if constexpr (kFp8) {
+#pragma unroll
+        for (int i = 0; i < NC; ++i) rref[i] = ms->ref[16 * (i / 4) + col0 + (i % 4)];
+      }
       if (t >= 1) {
         // this warp: value blocks 2 grp and 2 grp + 1 of its lane quadrant
         fail = !warp_wait(&ms->pt_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, p);
@@ -446,9 +472,8 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
     auto make_p = [&]() {
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
-        const int n0 = 16 * c + col0;
-        const float4 rr = *reinterpret_cast<const float4*>(&ms->ref[n0]);
-        const float rrv[4] = {rr.x, rr.y, rr.z, rr.w};
+        float rrv[4];
+        ref4(c, rrv);
         if (unmasked) {  // no masked score (a reference may still be -inf: then a move follows)
 #pragma unroll
           for (int j = 0; j < 4; ++j) pv[4 * c + j] = ex2(x[4 * c + j] - rrv[j]);
