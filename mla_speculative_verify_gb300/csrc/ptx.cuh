@@ -50,19 +50,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test for the completion of the phase with the given parity (no suspend):
-// for a thread that polls several barriers in turn.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 // The same test with acquire semantics at cluster scope: a phase completed by arrivals
 // from another CTA of the cluster (mbar_arrive_remote) makes that CTA's earlier writes to
 // this CTA's shared memory visible to the waiting thread.
