@@ -78,6 +78,19 @@ def test_plan_invariants(seq_lens, q_lens, H, num_sms):
     assert covered == hd["n_part_rows"]
     for m in p["merges"]:
         assert m["n_splits"] >= 2
+    # partial layout: split s of a row tile writes its rows at merge part_row0 + s * nrows + r,
+    # and every workspace partial row is written by exactly one unit
+    by_tile = {m["qrow0"]: m for m in p["merges"]}
+    written = []
+    for u in p["units"]:
+        if u["part_row0"] < 0:
+            assert u["n_splits"] == 1
+            continue
+        m = by_tile[u["qrow0"]]
+        assert m["nrows"] == u["nrows"] and m["n_splits"] == u["n_splits"]
+        assert u["part_row0"] == m["part_row0"] + u["split"] * u["nrows"]
+        written += [u["part_row0"] + r for r in range(u["nrows"])]
+    assert sorted(written) == list(range(hd["n_part_rows"]))
     # bf16 partial O rows (1 KB each) and fp32 partial LSE, each block 256-byte aligned
     assert ws == (0 if hd["n_part_rows"] == 0 else
                   ((hd["n_part_rows"] * 512 * 2 + 255) // 256 * 256 + (hd["n_part_rows"] * 4 + 255) // 256 * 256))
