@@ -229,9 +229,10 @@ struct SoftmaxArgs {
 
 // Softmax warps for a tile of 16 NCH packed rows. Warp (qd, grp) owns the 16 key rows of
 // TMEM lane quadrant qd (the M = 64 accumulator uses 16 lanes per quadrant) and, of every
-// 16 columns, the 8 columns 8 grp .. 8 grp + 7: lanes 0..15 read them from TMEM and hand
-// the upper 4 to lanes 16..31, so each thread works on 4 NCH columns of one key: columns
-// 16 c + 8 grp + 4 half + j, c < NCH, j < 4.
+// 16 columns, the 8 columns 8 grp .. 8 grp + 7, which one 16-lane TMEM load (16x256b)
+// spreads over all 32 threads: thread t holds keys kr0 = 16 qd + t / 4 and kr0 + 8 at columns
+// 16 c + cp and 16 c + cp + 1, cp = 8 grp + 2 (t % 4). Element x[4 c + j] is key kr0 + 8 (j / 2),
+// column 16 c + cp + j % 2 (c < NCH, j < 4).
 // Returns whether this thread issued O^T MMAs (lane 0 of softmax warps 0..3).
 template <int NCH, bool kFp8>
 __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params& p) {
@@ -241,9 +242,8 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
   constexpr float kMoveAbove = (kFp8 ? kRefSlackFp8 : kRefSlack) + kPShift;  // score - stored ref
   Misc* ms = a.ms;
   const int lane = a.lane, qd = a.qd, grp = a.grp, sidx = a.sidx;
-  const int half = lane >> 4;
-  const int krow = qd * 16 + (lane & 15);  // key row of this thread in the 64-key tile
-  const int col0 = 8 * grp + 4 * half;     // first of this thread's 4 columns in each chunk
+  const int kr0 = qd * 16 + (lane >> 2);  // this thread's first key row in the 64-key tile (second: kr0 + 8)
+  const int cp = 8 * grp + 2 * (lane & 3);  // first of this thread's 2 columns in each 16-column chunk
   const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
   const int w8 = sidx >> 5;              // softmax warp 0..7; warps 0..3 issue O^T block w8
   bool issued_ot = false;
@@ -329,27 +329,29 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
   bool fail = false;
   int lim_min = a.kv_end;
   for (int n = 0; n < a.nrows; ++n) lim_min = min(lim_min, ms->lim[n]);
+  constexpr int NP = 2 * NCH;  // this thread's columns (rows of the tile): 16 c + cp + k, index 2 c + k
   float l_acc[NC];
-  // e4m3: this thread's copies of its rows' references (they change only when a row
+  // e4m3: this thread's copies of its columns' references (they change only when a row
   // moves), so the shared-memory pipe, which the e4m3 path fills, serves fewer loads; the
   // bf16 path reads them from shared memory (its registers are spoken for)
-  float rref[kFp8 ? NC : 1];
+  float rref[kFp8 ? NP : 1];
 #pragma unroll
   for (int i = 0; i < NC; ++i) l_acc[i] = 0.f;
 #pragma unroll
-  for (int i = 0; i < (kFp8 ? NC : 1); ++i) rref[i] = -INFINITY;
-  // e4m3: the rows' score scales (fixed for the unit; the barrier above published them)
-  float csr[kFp8 ? NC : 1];
+  for (int i = 0; i < (kFp8 ? NP : 1); ++i) rref[i] = -INFINITY;
+  // e4m3: the columns' score scales (fixed for the unit; the barrier above published them)
+  float csr[kFp8 ? NP : 1];
 #pragma unroll
-  for (int i = 0; i < (kFp8 ? NC : 1); ++i)
-    csr[i] = kFp8 ? ms->colscale[16 * (i / 4) + col0 + (i % 4)] : 0.f;
+  for (int i = 0; i < (kFp8 ? NP : 1); ++i) csr[i] = kFp8 ? ms->colscale[16 * (i / 2) + cp + (i % 2)] : 0.f;
+  // the references of chunk c's two columns, r[j] for element 4 c + j
   auto ref4 = [&](int c, float* r) {
     if constexpr (kFp8) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) r[j] = rref[4 * c + j];
+      r[0] = r[2] = rref[2 * c];
+      r[1] = r[3] = rref[2 * c + 1];
     } else {
-      const float4 rr = *reinterpret_cast<const float4*>(&ms->ref[16 * c + col0]);
-      r[0] = rr.x; r[1] = rr.y; r[2] = rr.z; r[3] = rr.w;
+      const float2 rr = *reinterpret_cast<const float2*>(&ms->ref[16 * c + cp]);
+      r[0] = r[2] = rr.x;
+      r[1] = r[3] = rr.y;
     }
   };
   const float scale = p.score_scale_log2;
@@ -364,65 +366,64 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
     if (!fail) {
       ptx::tc_fence_after();
       // S^T: e4m3: the sum of the Q_hi and Q_lo column blocks of buffer t % 2; bf16: the
-      // sum of the three partials. Lanes 0..15 read 8 columns, lanes 16..31 take 4 of them
+      // sum of the three partials. All loads are issued before the one wait
       const uint32_t sbase = a.tmem + kTmemS + (kFp8 ? 128 * sb : 0) + lane_off + 8 * grp;
+      float s1[NC];
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
-        float s0[8], s1[8];
-        ptx::tmem_ld8(sbase + 16 * c, s0);
-        ptx::tmem_ld8(sbase + (kFp8 ? 16 * NCH : 64) + 16 * c, s1);
-        if constexpr (kFp8) {
-          ptx::tmem_ld_wait();
+        ptx::tmem_ld_16x256b(sbase + 16 * c, &x[4 * c]);
+        ptx::tmem_ld_16x256b(sbase + (kFp8 ? 16 * NCH : 64) + 16 * c, &s1[4 * c]);
+      }
+      if constexpr (kFp8) {
+        ptx::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) s0[j] += s1[j];
-        } else {
-          float s2[8];
-          ptx::tmem_ld8(sbase + 128 + 16 * c, s2);
-          ptx::tmem_ld_wait();
+        for (int i = 0; i < NC; ++i) x[i] += s1[i];
+      } else {
+        float s2[NC];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) s0[j] = (s0[j] + s1[j]) + s2[j];
-        }
+        for (int c = 0; c < NCH; ++c) ptx::tmem_ld_16x256b(sbase + 128 + 16 * c, &s2[4 * c]);
+        ptx::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float hi = __shfl_sync(0xffffffffu, s0[4 + j], lane & 15);
-          x[4 * c + j] = half ? hi : s0[j];
-        }
+        for (int i = 0; i < NC; ++i) x[i] = (x[i] + s1[i]) + s2[i];
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&ms->s_empty[s_buf]);
-      const int key = a.kv_begin + t * kTileKeys + krow;
+      const int key0 = a.kv_begin + t * kTileKeys + kr0;  // and key0 + 8
       const int tile_last = a.kv_begin + t * kTileKeys + kTileKeys - 1;
       unmasked = tile_last < a.kv_end && tile_last < lim_min;  // tile-uniform fast path
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
-        const int n0 = 16 * c + col0;
+        const int n0 = 16 * c + cp;
         float rrv[4];
         ref4(c, rrv);
         float csv[4] = {scale, scale, scale, scale};
         if constexpr (kFp8) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) csv[j] = csr[4 * c + j];
+          csv[0] = csv[2] = csr[2 * c];
+          csv[1] = csv[3] = csr[2 * c + 1];
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           float v = x[4 * c + j] * csv[j];
-          if (!unmasked) v = (key < a.kv_end && key < ms->lim[n0 + j]) ? v : -INFINITY;
+          const int key = key0 + 8 * (j >> 1);
+          if (!unmasked) v = (key < a.kv_end && key < ms->lim[n0 + (j & 1)]) ? v : -INFINITY;
           x[4 * c + j] = v;
           need |= v > rrv[j] + kMoveAbove;
         }
       }
     }
     // Moving the references (rare once a row has seen its largest scores): column maxima
-    // over this tile's keys (16 keys per half-warp), each row's reference up to its maximum,
-    // l and O^T (tiles < t, once PV(t-1) is done) rescaled by alpha.
+    // over this tile's keys (the quadrant's 16 keys: 2 per thread, 8 threads per column),
+    // each row's reference up to its maximum, l and O^T (tiles < t, once PV(t-1) is done)
+    // rescaled by alpha.
     auto move_refs = [&]() {
 #pragma unroll
-      for (int i = 0; i < NC; ++i) {
-        float m = x[i];
+      for (int i = 0; i < NP; ++i) {
+        const int c = i >> 1, k = i & 1;
+        float m = fmaxf(x[4 * c + k], x[4 * c + k + 2]);
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if ((lane & 15) == 0) ms->colred[qd][16 * (i / 4) + col0 + (i % 4)] = m;
+        for (int o = 4; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((lane >> 2) == 0) ms->colred[qd][16 * c + cp + k] = m;
       }
       softmax_sync();
       if (sidx < 16 * NCH) {
@@ -434,10 +435,10 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
       }
       softmax_sync();
 #pragma unroll
-      for (int i = 0; i < NC; ++i) l_acc[i] *= ms->alpha[16 * (i / 4) + col0 + (i % 4)];
+      for (int i = 0; i < NC; ++i) l_acc[i] *= ms->alpha[16 * (i / 4) + cp + (i & 1)];
       if constexpr (kFp8) {
 #pragma unroll
-        for (int i = 0; i < NC; ++i) rref[i] = ms->ref[16 * (i / 4) + col0 + (i % 4)];
+        for (int i = 0; i < NP; ++i) rref[i] = ms->ref[16 * (i / 2) + cp + (i % 2)];
       }
       if (t >= 1) {
         // this warp: value blocks 2 grp and 2 grp + 1 of its lane quadrant
@@ -467,8 +468,8 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
     // probabilities relative to the current references (pv, kept until l takes them),
     // packed to bf16, or for the e4m3 path times 2^4 and split into hi + lo e4m3 parts
     float pv[NC];
-    uint32_t pk[NC / 2];
-    uint32_t ph[NCH], pl[NCH];
+    uint32_t pk[NC / 2];           // bf16: pk[2 c + k] = the 2 columns of key kr0 + 8 k in chunk c
+    uint32_t ph[NC / 2], pl[NC / 2];  // e4m3: the same pairs as hi and lo bytes (low 16 bits)
     auto make_p = [&]() {
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
@@ -485,11 +486,8 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
           }
         }
         if constexpr (kFp8) {
-          uint32_t h01, l01, h23, l23;
-          split_e4m3x2(pv[4 * c], pv[4 * c + 1], h01, l01);
-          split_e4m3x2(pv[4 * c + 2], pv[4 * c + 3], h23, l23);
-          ph[c] = h01 | (h23 << 16);
-          pl[c] = l01 | (l23 << 16);
+          split_e4m3x2(pv[4 * c], pv[4 * c + 1], ph[2 * c], pl[2 * c]);
+          split_e4m3x2(pv[4 * c + 2], pv[4 * c + 3], ph[2 * c + 1], pl[2 * c + 1]);
         } else {
           pk[2 * c] = pack_bf16(pv[4 * c], pv[4 * c + 1]);
           pk[2 * c + 1] = pack_bf16(pv[4 * c + 2], pv[4 * c + 3]);
@@ -497,34 +495,32 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
       }
     };
     auto store_p = [&]() {
-      if constexpr (kFp8) {
-        // e4m3 P^T hi and lo, MN-major with 64-byte rows (64-byte swizzle): key krow's row
-        uint8_t* line_hi = a.sPt + sb * kPtBytes + krow * 64;
-        uint8_t* line_lo = line_hi + kTileKeys * 64;
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          const int off = (((c ^ (krow >> 1)) & 3) << 4) + col0;
-          *reinterpret_cast<uint32_t*>(line_hi + off) = ph[c];
-          *reinterpret_cast<uint32_t*>(line_lo + off) = pl[c];
+      for (int k = 0; k < 2; ++k) {
+        const int kr = kr0 + 8 * k;
+        if constexpr (kFp8) {
+          // e4m3 P^T hi and lo, MN-major with 64-byte rows (64-byte swizzle): key kr's row
+          uint8_t* line_hi = a.sPt + sb * kPtBytes + kr * 64;
+          uint8_t* line_lo = line_hi + kTileKeys * 64;
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            const int off = (((c ^ (kr >> 1)) & 3) << 4) + cp;
+            *reinterpret_cast<uint16_t*>(line_hi + off) = (uint16_t)ph[2 * c + k];
+            *reinterpret_cast<uint16_t*>(line_lo + off) = (uint16_t)pl[2 * c + k];
+          }
+        } else {
+          uint8_t* line = a.sPt + sb * kPtBytes + kr * 128;
+#pragma unroll
+          for (int c = 0; c < NCH; ++c)
+            *reinterpret_cast<uint32_t*>(line + ((((2 * c + grp) ^ (kr & 7)) & 7) << 4) + 4 * (lane & 3)) = pk[2 * c + k];
         }
-      } else {
-        uint8_t* line = a.sPt + sb * kPtBytes + krow * 128;
+        if (a.kv_begin + t * kTileKeys + kr >= a.kv_end) {
+          // a cache slot past the key range: zero its value columns so P = 0 meets V = 0 (the
+          // 8 threads holding key kr take one of its 8 value chunks each: 4 grp + t % 4)
+          uint8_t* row = a.sKv + (t % G::kStages) * G::kSlot + kr * G::kRowBytes + (4 * grp + (lane & 3)) * G::kChunkBytes;
 #pragma unroll
-        for (int c = 0; c < NCH; ++c)
-          *reinterpret_cast<uint2*>(line + ((((2 * c + grp) ^ (krow & 7)) & 7) << 4) + 8 * half) =
-              make_uint2(pk[2 * c], pk[2 * c + 1]);
-      }
-      const int key = a.kv_begin + t * kTileKeys + krow;
-      if (key >= a.kv_end) {
-        // a cache slot past the key range: zero its value columns so P = 0 meets V = 0 (this
-        // thread: chunks 2 q4 and 2 q4 + 1, q4 = 2 grp + half)
-        uint8_t* row = a.sKv + (t % G::kStages) * G::kSlot + krow * G::kRowBytes;
-        const int q4 = 2 * grp + half;
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int j = 0; j < G::kRowBytes / 16; ++j)
-            *reinterpret_cast<uint4*>(row + (2 * q4 + c) * G::kChunkBytes + 16 * j) = make_uint4(0, 0, 0, 0);
+          for (int j = 0; j < G::kRowBytes / 16; ++j) *reinterpret_cast<uint4*>(row + 16 * j) = make_uint4(0, 0, 0, 0);
+        }
       }
       ptx::fence_async_smem();
       ptx::tc_fence_before();
@@ -596,11 +592,12 @@ __device__ __forceinline__ bool softmax_role(const SoftmaxArgs& a, const Params&
   // the last tile's O^T MMAs. The wait for those MMAs and the abort vote come after.
   if (!stop) {
 #pragma unroll
-    for (int i = 0; i < NC; ++i) {
-      float s = l_acc[i];
+    for (int i = 0; i < NP; ++i) {
+      const int c = i >> 1, k = i & 1;
+      float s = l_acc[4 * c + k] + l_acc[4 * c + k + 2];
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if ((lane & 15) == 0) ms->colred[qd][16 * (i / 4) + col0 + (i % 4)] = s;
+      for (int o = 4; o < 32; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if ((lane >> 2) == 0) ms->colred[qd][16 * c + cp + k] = s;
     }
     softmax_sync();
     if (sidx < 64) {
