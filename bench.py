@@ -99,14 +99,20 @@ def algorithmic_flops(prob) -> float:
 
 
 def kernel_source_hash() -> str:
-    """sha256[:16] over the library's CUDA sources (sorted), recorded in each ncu summary."""
+    """sha256[:16] over the library's CUDA sources (sorted), recorded in each ncu summary.
+    Comments and whitespace are left out (the sources hold no "//" or "/*" inside string
+    literals), so a change to the code changes it and an edit of a comment does not."""
     import hashlib
+    import re
 
     h = hashlib.sha256()
     for name in sorted(os.listdir(CSRC)):
         if name.endswith((".cu", ".cuh", ".h")):
+            text = open(os.path.join(CSRC, name)).read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
             h.update(name.encode())
-            h.update(open(os.path.join(CSRC, name), "rb").read())
+            h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

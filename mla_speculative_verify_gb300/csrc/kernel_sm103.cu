@@ -16,38 +16,38 @@
 // MN-major (the latent cache rows hold V in columns 0..511; flashinfer PR #5602 "What
 // r52 changes": the latent K stages are held until PV).
 //
-// One thread issues a tcgen05.mma only every ~100 cycles (~120 for the MN-major and e4m3
-// forms), whatever the MMA's N, while an N = 16..96 MMA needs 8..48 cycles of tensor time,
-// so the products of a page are issued from several threads: three MMA warps split the
-// K-steps of S^T into one accumulator (the first K-step, which overwrites it, comes from
-// the leader before the others start), and O^T, zeroed in tensor memory at the start of
-// the unit so that every O^T MMA accumulates, is issued by four softmax warps (one value
-// block each) for a bf16 cache, or shared by the three MMA warps for an e4m3 cache. For an
-// e4m3 cache each S^T K-step multiplies the page by Q_hi and Q_lo at once (N = 2 nmma).
-// S^T is double-buffered in tensor memory, so the product of the next page runs while the
-// softmax works on this one.
+// One thread issues a tcgen05.mma only every ~65-125 cycles (the form and the operand
+// layouts), whatever the MMA's N, while an N = 16..96 MMA needs 8..48 cycles of tensor time,
+// so the products of a page are issued from several threads, each into accumulators no
+// other thread writes (so a unit's result is the same bit for bit on every run). O^T is
+// zeroed in tensor memory at the start of the unit, so every O^T MMA accumulates.
+//   bf16 cache:  three MMA warps each issue a third of the 36 S^T K-steps into a partial
+//                accumulator of their own (the softmax adds the three); one S^T buffer, so
+//                the next page's product starts as soon as the softmax has read this one.
+//                O^T is issued by four of the softmax warps, one value block each.
+//   e4m3 cache:  each S^T K-step multiplies the page by Q_hi and Q_lo at once (N = 2 nmma);
+//                two MMA warps take alternate pages into two S^T buffers; O^T value blocks
+//                0-1 come from an O^T warp, blocks 2-3 from the producer warp.
 //
 // Warp roles (one CTA per SM):
 //   warp 0     TMA producer: the Q tile once (bf16 cache), then one page per stage
 //              (two bf16 stages, or four e4m3 stages, in the same ring), each copy with
 //              an L2 prefetch of the page that enters the ring next (bf16: those of the
-//              first S copies leave once page 0 has landed)
-//   warps 1-3  MMA warps: a third of the K-steps of S^T(t) each, into buffer t % 2; for an
-//              e4m3 cache also a third of the MMAs of O^T(t - 1) += V^T P^T(t - 1). Warp 1
-//              leads: it does the waits, and the three vote on a named barrier
-//   warps 4-11 softmax: each thread owns one key of the S^T tile (a TMEM lane) and a
-//              quarter of the columns of each 16-column chunk; online
-//              softmax with a lazy per-row reference: the reference moves, and O^T is
-//              rescaled in TMEM, only when a score exceeds it by a few octaves (the
-//              conditional rescale of flashinfer PR #5602); then the epilogue: O / l to
-//              bf16 out and LSE, or bf16 partials for the merge kernel. The eight warps
-//              agree on every decision through OR-reducing named barriers. For a bf16
-//              cache P^T(t) is written with the current references first, so that one
-//              barrier per tile both votes on reference moves and closes P^T(t) (a move
-//              rewrites it); after it four of the warps each issue one value block of
-//              O^T(t) += V^T P^T(t). (On the critical path of the two-stage bf16 page ring
-//              this saves a wake-up; the e4m3 softmax is already the busiest role, so there
-//              the MMA warps do it.)
+//              first S copies leave once page 0 has landed); e4m3: also O^T blocks 2-3
+//   warps 1-3  MMA warps (above)
+//   warps 4-11 softmax: warp (quadrant qd, group grp) owns the 16 keys of TMEM lane
+//              quadrant qd and 8 of every 16 columns; a 16-lane TMEM load gives each
+//              thread 2 keys x 2 columns. Online softmax with a lazy per-row reference:
+//              the reference moves, and O^T is rescaled in TMEM, only when a score exceeds
+//              it by a few octaves (the conditional rescale of flashinfer PR #5602); then
+//              the epilogue: O / l to bf16 out and LSE, or bf16 partials for the merge
+//              kernel. The eight warps agree on every decision through OR-reducing named
+//              barriers. For a bf16 cache P^T(t) is written with the current references
+//              first, so that one barrier per tile both votes on reference moves and closes
+//              P^T(t) (a move rewrites it); after it four of the warps each issue one value
+//              block of O^T(t) += V^T P^T(t). (On the critical path of the two-stage bf16
+//              page ring this saves a wake-up; the e4m3 softmax is already the busiest role,
+//              so there other warps do it.)
 //
 // For an e4m3 cache the products run on kind::f8f6f4 MMAs straight from the cached
 // codes: each Q row is scaled by a power of two and split into two e4m3 parts (hi and
