@@ -502,26 +502,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tp = i + kStages;
         const int page_pf = __shfl_sync(0xffffffffu, tp < 32 ? pid_cur : pid_next, tp & 31);
         const int t = t0 + i, slot = t % kStages;
-        int ok = 1;
-        if (lane == 0) {
-          // the slot of page t - S is free once O^T(t - S) is done
-          if (t >= kStages) ok = wait_bar(&ms->kv_empty[slot], ((t - kStages) / kStages) & 1, abort, p);
-          if (ok && !(blockIdx.x == 0 && t == p.skip_copy)) {
-            uint8_t* dst = sKv + slot * kSlot;
-            ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], kSlot);
-            if (read_once)
-              ptx::tma_load_3d_hint(dst, &tkv4, &ms->kv_full[slot], 0, page * kPage, 4 * (int)crank, pol);
-            else
-              ptx::tma_load_3d(dst, &tkv4, &ms->kv_full[slot], 0, page * kPage, 4 * (int)crank);
-            ptx::tma_load_3d(dst + 4 * kChunkBytes, &tkv1, &ms->kv_full[slot], 0, page * kPage, 8);
-            if (t0 + tp < ntiles) {
-              ptx::tma_prefetch_l2_3d(&tkv4, 0, page_pf * kPage, 4 * (int)crank);
-              ptx::tma_prefetch_l2_3d(&tkv1, 0, page_pf * kPage, 8);
-            }
+        // the slot of page t - S is free once O^T(t - S) is done (the whole warp waits)
+        if (t >= kStages && !warp_wait(&ms->kv_empty[slot], ((t - kStages) / kStages) & 1, abort, p)) break;
+        if (lane == 0 && !(blockIdx.x == 0 && t == p.skip_copy)) {
+          uint8_t* dst = sKv + slot * kSlot;
+          ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], kSlot);
+          if (read_once)
+            ptx::tma_load_3d_hint(dst, &tkv4, &ms->kv_full[slot], 0, page * kPage, 4 * (int)crank, pol);
+          else
+            ptx::tma_load_3d(dst, &tkv4, &ms->kv_full[slot], 0, page * kPage, 4 * (int)crank);
+          ptx::tma_load_3d(dst + 4 * kChunkBytes, &tkv1, &ms->kv_full[slot], 0, page * kPage, 8);
+          if (t0 + tp < ntiles) {
+            ptx::tma_prefetch_l2_3d(&tkv4, 0, page_pf * kPage, 4 * (int)crank);
+            ptx::tma_prefetch_l2_3d(&tkv1, 0, page_pf * kPage, 8);
           }
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
+        __syncwarp();
         issued = t + 1;
       }
       pid_cur = pid_next;

@@ -743,20 +743,24 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
         return pid;
       };
       auto load_ids = [&](int t0) { return checked(t0 + lane < ntiles ? pt_row[t0 + lane] : 0, t0 + lane); };
-      // e4m3 (lane 0): O^T(u) += V^T . P^T(u) for value blocks 2 and 3, once P^T(u) is written
+      // e4m3: O^T(u) += V^T . P^T(u) for value blocks 2 and 3, once P^T(u) is written (the
+      // whole warp waits, lane 0 issues)
       auto producer_ot = [&](int u) -> int {
-        if (!wait_bar(&ms->p_full[u & 1], (u >> 1) & 1, abort, p)) return 0;
+        if (!warp_wait(&ms->p_full[u & 1], (u >> 1) & 1, abort, p)) return 0;
         ptx::tc_fence_after();
-        const uint32_t skv = ptx::smem_addr(sKv), spt = ptx::smem_addr(sPt);
+        if (lane == 0) {
+          const uint32_t skv = ptx::smem_addr(sKv), spt = ptx::smem_addr(sPt);
 #pragma unroll
-        for (int blk = 2; blk < 4; ++blk)
+          for (int blk = 2; blk < 4; ++blk)
 #pragma unroll
-          for (int k = 0; k < 2; ++k)
+            for (int k = 0; k < 2; ++k)
 #pragma unroll
-            for (int part = 0; part < 2; ++part) issue_ot_mma_e4m3(tmem, skv, spt, u, nmma, blk, k, part);
-        ptx::mma_commit(&ms->kv_empty[u % S]);
-        ptx::mma_commit(&ms->pt_empty[u & 1]);
-        ot_issued = true;
+              for (int part = 0; part < 2; ++part) issue_ot_mma_e4m3(tmem, skv, spt, u, nmma, blk, k, part);
+          ptx::mma_commit(&ms->kv_empty[u % S]);
+          ptx::mma_commit(&ms->pt_empty[u & 1]);
+          ot_issued = true;
+        }
+        __syncwarp();
         return 1;
       };
       // a page that only this row tile reads may leave L2 first once it is in shared
@@ -772,23 +776,22 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
           const int tp = i + S;  // the page after the ring (index relative to t0)
           const int page_pf = __shfl_sync(0xffffffffu, tp < 32 ? pid_cur : pid_next, tp & 31);
           const int t = t0 + i, slot = t % S;
-          int ok = 1;
-          if (lane == 0) {
-            // e4m3: this warp also issues value blocks 2 and 3 of O^T(t - S), the page whose
-            // slot the copy of page t reuses (blocks 0 and 1 come from the O^T warp)
-            if (kFp8 && t >= S) ok = producer_ot(t - S);
-            if (ok && t >= S) ok = wait_bar(&ms->kv_empty[slot], ((t - S) / S) & 1, abort, p);
-            if (ok && !(blockIdx.x == 0 && t == p.skip_copy)) {
-              ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], G::kSlot);
-              if (read_once)
-                ptx::tma_load_3d_hint(sKv + slot * G::kSlot, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0, pol);
-              else
-                ptx::tma_load_3d(sKv + slot * G::kSlot, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0);
-              if ((kFp8 || t >= S) && t0 + tp < ntiles) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, page_pf * kPage, 0);
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
+          // e4m3: this warp also issues value blocks 2 and 3 of O^T(t - S), the page whose
+          // slot the copy of page t reuses (blocks 0 and 1 come from the O^T warp). The
+          // waits are the whole warp's; lane 0 issues.
+          bool ok = true;
+          if (kFp8 && t >= S) ok = producer_ot(t - S) != 0;
+          if (ok && t >= S) ok = warp_wait(&ms->kv_empty[slot], ((t - S) / S) & 1, abort, p);
           if (!ok) break;
+          if (lane == 0 && !(blockIdx.x == 0 && t == p.skip_copy)) {
+            ptx::mbar_arrive_expect_tx(&ms->kv_full[slot], G::kSlot);
+            if (read_once)
+              ptx::tma_load_3d_hint(sKv + slot * G::kSlot, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0, pol);
+            else
+              ptx::tma_load_3d(sKv + slot * G::kSlot, &tmap_kv, &ms->kv_full[slot], 0, page * kPage, 0);
+            if ((kFp8 || t >= S) && t0 + tp < ntiles) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, page_pf * kPage, 0);
+          }
+          __syncwarp();
           issued = t + 1;
           if (!kFp8 && t == S - 1) {
             // bf16: the prefetches that go with the first S copies leave once page 0 has
@@ -796,11 +799,12 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
             int pf[S];
 #pragma unroll
             for (int k = 0; k < S; ++k) pf[k] = __shfl_sync(0xffffffffu, pid_cur, S + k);
-            if (lane == 0 && wait_bar(&ms->kv_full[0], 0, abort, p)) {
+            if (warp_wait(&ms->kv_full[0], 0, abort, p) && lane == 0) {
 #pragma unroll
               for (int k = 0; k < S; ++k)
                 if (S + k < ntiles) ptx::tma_prefetch_l2_3d(&tmap_kv, 0, pf[k] * kPage, 0);
             }
+            __syncwarp();
           }
         }
         pid_cur = pid_next;
@@ -809,9 +813,7 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
       // e4m3: blocks 2 and 3 of O^T for the last S pages (no copy follows them)
       if (kFp8 && issued == ntiles) {
         int ok = 1;
-        if (lane == 0)
-          for (int u = max(0, ntiles - S); ok && u < ntiles; ++u) ok = producer_ot(u);
-        __syncwarp();
+        for (int u = max(0, ntiles - S); ok && u < ntiles; ++u) ok = producer_ot(u);
       }
     }
     // Drain: every issued copy must land before the CTA may exit (at most the last S
