@@ -940,13 +940,16 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1)
 }
 
 // ------------------------------------------------------------------ LSE merge
-// One CTA per (packed row, quarter of the 512 value columns): its W warps (4, 8 or 16,
-// enough for all splits at kMergeBatch loads per lane) share the splits of the row; fewer
-// warps per CTA let more CTAs share an SM. L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s.
+// One CTA per (packed row, slice of the 512 value columns: SL = 4 slices of 128 columns, or
+// 8 of 64 when the merge has few rows, so that more SMs share its loads): its W warps (4, 8
+// or 16, enough for all splits at kMergeBatch loads per lane) share the splits of the row;
+// fewer warps per CTA let more CTAs share an SM. L = ln sum_s exp(L_s),
+// O = sum_s exp(L_s - L) O_s.
 constexpr int kMergeThreads = 512;
 constexpr int kMergeWarps = kMergeThreads / 32;
 constexpr int kMergeBatch = 10;  // partial-O loads in flight per lane (16 warps x 10 = 160 splits per round trip)
 constexpr int kMergeMaxSplits = 2048;
+constexpr long long kMergeWideSlicesMaxCtas = 200;  // 8 slices per row up to this many merge CTAs
 
 // Four bf16 partial-O values (8 bytes, streamed: read once) as fp32.
 __device__ __forceinline__ float4 load_part4(const __nv_bfloat16* ptr) {
@@ -958,20 +961,22 @@ __device__ __forceinline__ float4 load_part4(const __nv_bfloat16* ptr) {
 
 // 64 registers per thread (the minimum-blocks bound): two 16-warp CTAs per SM, so the
 // merge CTAs of a 48-row tile with ~150 splits (192 of them) run in one wave.
-template <int W>
+template <int W, int SL>
 __global__ void __launch_bounds__(32 * W, 1024 / (32 * W)) lse_merge_kernel(const PlanMerge* merges, const __nv_bfloat16* part_o,
                                                                  const float* part_lse, __nv_bfloat16* out, float* lse) {
+  static_assert(SL == 4 || SL == 8, "4 or 8 column slices per row");
+  constexpr int kCols = kDv / SL / 32;  // value columns per lane: 4 or 2
   __shared__ float m_s[W], l_s[W];
   __shared__ float4 acc_s[W][32];
   // the merge item is plan data, written before the fold kernel ran: read it while the
   // fold kernel finishes, then wait for the partials
   const PlanMerge m = merges[blockIdx.y];
   ptx::pdl_wait_primary();
-  const int row = blockIdx.x >> 2, quarter = blockIdx.x & 3;
+  const int row = blockIdx.x / SL, slice = blockIdx.x % SL;
   if (row >= m.nrows) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ns = m.n_splits;  // the planner keeps this <= kMergeMaxSplits
-  const int col = quarter * 128 + 4 * lane;
+  const int col = slice * (kDv / SL) + kCols * lane;
   const __nv_bfloat16* base = part_o + (size_t)(m.part_row0 + row) * kDv + col;
   const size_t split_stride = (size_t)m.nrows * kDv;
   // Warp w folds its splits w, w + W, ... into a running (max M_w, sum l_w = sum_s e^(L_s -
@@ -981,12 +986,17 @@ __global__ void __launch_bounds__(32 * W, 1024 / (32 * W)) lse_merge_kernel(cons
   float mw = -INFINITY, lw = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s0 = warp; s0 < ns; s0 += W * kMergeBatch) {
-    uint2 v[kMergeBatch];  // four bf16 partial-O values each, unpacked when used
+    uint2 v[kMergeBatch];  // kCols bf16 partial-O values each, unpacked when used
     float x[kMergeBatch];
 #pragma unroll
     for (int u = 0; u < kMergeBatch; ++u) {
       const int s = s0 + W * u;
-      v[u] = s < ns ? __ldcs(reinterpret_cast<const uint2*>(base + (size_t)s * split_stride)) : make_uint2(0u, 0u);
+      if constexpr (kCols == 4) {
+        v[u] = s < ns ? __ldcs(reinterpret_cast<const uint2*>(base + (size_t)s * split_stride)) : make_uint2(0u, 0u);
+      } else {
+        v[u].x = s < ns ? __ldcs(reinterpret_cast<const unsigned int*>(base + (size_t)s * split_stride)) : 0u;
+        v[u].y = 0u;
+      }
       x[u] = s < ns ? part_lse[m.part_row0 + s * m.nrows + row] : -INFINITY;
     }
     float mb = mw;
@@ -1000,9 +1010,12 @@ __global__ void __launch_bounds__(32 * W, 1024 / (32 * W)) lse_merge_kernel(cons
     for (int u = 0; u < kMergeBatch; ++u) {
       const float w = x[u] == -INFINITY ? 0.f : __expf(x[u] - mb);
       const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[u].x));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[u].y));
       lw += w;
-      acc.x += w * a.x; acc.y += w * a.y; acc.z += w * b.x; acc.w += w * b.y;
+      acc.x += w * a.x; acc.y += w * a.y;
+      if constexpr (kCols == 4) {
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[u].y));
+        acc.z += w * b.x; acc.w += w * b.y;
+      }
     }
     mw = mb;
   }
@@ -1031,9 +1044,12 @@ __global__ void __launch_bounds__(32 * W, 1024 / (32 * W)) lse_merge_kernel(cons
     }
     const float inv = 1.f / l;
     const int qr = m.qrow0 + row;
-    *reinterpret_cast<uint2*>(out + (size_t)qr * kDv + col) =
-        make_uint2(pack_bf16(r.x * inv, r.y * inv), pack_bf16(r.z * inv, r.w * inv));
-    if (lse && quarter == 0 && lane == 0) lse[qr] = M + __logf(l);
+    if constexpr (kCols == 4)
+      *reinterpret_cast<uint2*>(out + (size_t)qr * kDv + col) =
+          make_uint2(pack_bf16(r.x * inv, r.y * inv), pack_bf16(r.z * inv, r.w * inv));
+    else
+      *reinterpret_cast<uint32_t*>(out + (size_t)qr * kDv + col) = pack_bf16(r.x * inv, r.y * inv);
+    if (lse && slice == 0 && lane == 0) lse[qr] = M + __logf(l);
   }
 }
 
@@ -1245,9 +1261,13 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
     int max_ns = 0;
     for (int i = 0; i < h->n_merge; ++i) max_ns = max(max_ns, mh[i].n_splits);
     const bool small = max_ns <= kMergeSmallSplits;
+    // CTA-per-row merge: 8 column slices per row while that keeps the CTAs within about
+    // two-thirds of the SMs (a 12- or 24-row merge: its loads spread over twice the SMs),
+    // else 4 (more CTAs than that queue for SMs and cost more than they spread)
+    const int slices = (long long)h->rows_cap * 8 * h->n_merge <= kMergeWideSlicesMaxCtas ? 8 : 4;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = small ? dim3((unsigned)((h->rows_cap * 4 + kMergeSmallWarps - 1) / kMergeSmallWarps), (unsigned)h->n_merge, 1)
-                        : dim3((unsigned)(h->rows_cap * 4), (unsigned)h->n_merge, 1);
+                        : dim3((unsigned)(h->rows_cap * slices), (unsigned)h->n_merge, 1);
     // CTA-per-row merge: just enough warps for one round trip of loads (fewer registers per
     // CTA, so more of them fit on an SM as the fold kernel's CTAs leave)
     const int large_warps = max_ns <= 4 * kMergeBatch ? 4 : max_ns <= 8 * kMergeBatch ? 8 : kMergeWarps;
@@ -1259,12 +1279,15 @@ extern "C" int mla_decode_run(const void* plan_dev, const void* plan_host, size_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    ce = cudaLaunchKernelEx(&cfg,
-                            small ? lse_merge_small_kernel
-                                  : large_warps == 4 ? lse_merge_kernel<4>
-                                                     : large_warps == 8 ? lse_merge_kernel<8> : lse_merge_kernel<kMergeWarps>,
-                            (const PlanMerge*)((const uint8_t*)plan_dev + h->merge_off), (const __nv_bfloat16*)prm.part_o,
-                            (const float*)prm.part_lse, (__nv_bfloat16*)out, lse);
+    auto merge_fn = small ? lse_merge_small_kernel
+                    : slices == 8 ? (large_warps == 4   ? lse_merge_kernel<4, 8>
+                                     : large_warps == 8 ? lse_merge_kernel<8, 8>
+                                                        : lse_merge_kernel<kMergeWarps, 8>)
+                                  : (large_warps == 4   ? lse_merge_kernel<4, 4>
+                                     : large_warps == 8 ? lse_merge_kernel<8, 4>
+                                                        : lse_merge_kernel<kMergeWarps, 4>);
+    ce = cudaLaunchKernelEx(&cfg, merge_fn, (const PlanMerge*)((const uint8_t*)plan_dev + h->merge_off),
+                            (const __nv_bfloat16*)prm.part_o, (const float*)prm.part_lse, (__nv_bfloat16*)out, lse);
     if (ce != cudaSuccess) return set_error(MLA_ERR_CUDA, "merge kernel launch: %s", cudaGetErrorString(ce));
   }
   return MLA_OK;
