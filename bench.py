@@ -361,43 +361,59 @@ def visible_key_rows(seq_lens, q_lens, H) -> int:
     return n
 
 
-def oracle_sample(prob, tokens: int = 2):
+def oracle_sample(prob, tokens: int = 1, max_keys: int | None = None):
     """A bounded sample of one call for the float64 oracle: the first `tokens` verify
-    tokens of the first request, at its full context (token i keeps its causal key
-    range), and the factor that scales the sample's time to the whole call (visible
-    key-rows of the call over those of the sample)."""
+    tokens of the first request, against the first `max_keys` keys of its context (all of
+    them when None; token i keeps its causal key range within the sample), and the factor
+    that scales the sample's time to the whole call (visible key-rows of the call over
+    those of the sample)."""
     ctx, q = int(prob.seq_lens[0]), int(prob.q_lens[0])
     t = max(1, min(q, tokens))
-    sub = inputs.Problem(H=prob.H, seq_lens=np.array([ctx - q + t], np.int32), q_lens=np.array([t], np.int32),
+    keys = ctx - q + t if max_keys is None else max(t, min(ctx - q + t, int(max_keys)))
+    sub = inputs.Problem(H=prob.H, seq_lens=np.array([keys], np.int32), q_lens=np.array([t], np.int32),
                          page_table=prob.page_table[:1], q=prob.q[:t].clone(), kv=prob.kv, kv_dtype=prob.kv_dtype,
                          kv_scale=prob.kv_scale, sm_scale=prob.sm_scale)
     scale = visible_key_rows(prob.seq_lens, prob.q_lens, prob.H) / visible_key_rows(sub.seq_lens, sub.q_lens, prob.H)
     return sub, scale
 
 
-def cpu_baseline(probs, tokens: int = 2):
+REF_BUDGET_S = 150.0  # oracle seconds of a whole `--impl reference` run
+CAL_KEYS = 16384  # keys of the calibration sample that sizes each call's timed sample
+
+
+def cpu_baseline(probs, budget_s: float = 15.0):
     """The float64 oracle, as it stands (split + merge mode, 64 key chunks per request),
     on this host's cores, over a bounded sample of every call of the step: the first
-    `tokens` verify tokens of each call at full context, timed and scaled to the whole
-    call by its visible key-rows."""
+    verify token of each call against the first keys of its context, as many keys as fit
+    an equal share of `budget_s` seconds (a calibration sample of CAL_KEYS keys sets the
+    rate), timed and scaled to the whole call by its visible key-rows."""
     import oracle
 
     oracle.build()
     cores = os.cpu_count() or 1
-    us = []
-    for prob in probs:
-        sub, scale = oracle_sample(prob, tokens)
+
+    def timed(sub):
         kvd = oracle.KV_BF16 if sub.kv_dtype == inputs.KV_BF16 else oracle.KV_FP8_E4M3
         bounds = [sorted(set(int(c) * i // 64 for i in range(65))) for c in sub.seq_lens]
         t0 = time.perf_counter()
         oracle.decode(sub.q_bits(), sub.kv_bits(), kvd, sub.kv_scale, sub.page_table, sub.page_size,
                       sub.seq_lens, sub.q_lens, sub.H, sub.sm_scale, mode=oracle.MODE_SPLIT, split_bounds=bounds,
                       nthreads=cores)
-        us.append((time.perf_counter() - t0) * 1e6 * scale)
+        return time.perf_counter() - t0
+
+    us, keys = [], []
+    share = budget_s / max(1, len(probs))
+    for prob in probs:
+        cal, _ = oracle_sample(prob, 1, CAL_KEYS)
+        rate = timed(cal) / int(cal.seq_lens[0])  # seconds per key of one token
+        sub, scale = oracle_sample(prob, 1, max(CAL_KEYS, int(share / max(rate, 1e-12))))
+        keys.append(int(sub.seq_lens[0]))
+        us.append(timed(sub) * 1e6 * scale)
     return dict(us_per_call=float(np.mean(us)), cores=cores, calls=len(probs),
-                sample=(f"every call of the step ({len(probs)}), each on its first {tokens} verify tokens of the "
-                        "first request at full context, oracle split+merge mode; time scaled to the whole call by "
-                        "visible key-rows"))
+                sample=(f"every call of the step ({len(probs)}), each on its first verify token of the first "
+                        f"request against its first {min(keys)}..{max(keys)} keys (sized to ~{budget_s:.0f} s of "
+                        "oracle time per step), oracle split+merge mode; time scaled to the whole call by visible "
+                        "key-rows"))
 
 
 def max_over_ranks(x: float, device) -> float:
@@ -441,9 +457,11 @@ def main():
         # the oracle is the reference arm: rank 0 only, bounded samples per step
         if rank != 0:
             return
+        # each step a bounded sample, sized so that the whole run takes ~REF_BUDGET_S
+        budget = min(30.0, max(2.0, REF_BUDGET_S / (args.warmup + args.steps)))
         times = []
         for i in range(args.warmup + args.steps):
-            r = cpu_baseline(probs)
+            r = cpu_baseline(probs, budget)
             if i >= args.warmup:
                 times.append(r["us_per_call"])
         v = statistics.median(times)
