@@ -57,6 +57,9 @@ def workload(name: str):
     if name == "sweep131k":
         return [inputs.workload_sweep_131k(q) for q in (1, 2, 4, 8)], dict(
             workload="h12_ctx131072_bf16_q1-2-4-8", H=12, ctx=131072, q=[1, 2, 4, 8], kv="bf16", page_size=64)
+    if name == "sweep131k_fp8":
+        return [inputs.workload_sweep_131k(q, kv_dtype=inputs.KV_FP8) for q in (1, 2, 4, 8)], dict(
+            workload="h12_ctx131072_fp8_q1-2-4-8", H=12, ctx=131072, q=[1, 2, 4, 8], kv="fp8_e4m3", page_size=64)
     if name == "contig4096":
         return [inputs.workload_contiguous_small()], dict(workload="h12_q2_ctx4096_bf16_contiguous", H=12, ctx=4096,
                                                          q=[2], kv="bf16", page_size=64)

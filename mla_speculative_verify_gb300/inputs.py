@@ -158,9 +158,9 @@ def workload_contiguous_small(seed: int = 1001) -> Problem:
     return make_problem(12, [4096], [2], KV_BF16, seed, contiguous=True, name="h12_q2_ctx4096_bf16_contig")
 
 
-def workload_sweep_131k(q: int, ctx: int = 131072, seed: int = 1002) -> Problem:
-    """B=1, H=12, q in {1,2,4,8}, ctx=131072, bf16, random page table."""
-    return make_problem(12, [ctx], [q], KV_BF16, seed, name=f"h12_q{q}_ctx{ctx}_bf16")
+def workload_sweep_131k(q: int, ctx: int = 131072, seed: int = 1002, kv_dtype: str = KV_BF16) -> Problem:
+    """B=1, H=12, q in {1,2,4,8}, ctx=131072, bf16 (or fp8 e4m3), random page table."""
+    return make_problem(12, [ctx], [q], kv_dtype, seed, name=f"h12_q{q}_ctx{ctx}_{kv_dtype}")
 
 
 def workload_long(kv_dtype: str, ctx: int = 1 << 20, q: int = 8, seed: int = 1003) -> Problem:

@@ -179,9 +179,10 @@ def test_plan_mismatch_is_reported_not_faulted():
 
 
 # ---------------------------------------------------------------- full sizes, sampled tokens
-@pytest.mark.parametrize("q", [1, 8])
-def test_full_size_h12_131k_sampled(q):
-    prob = inputs.workload_sweep_131k(q)
+@pytest.mark.parametrize("q", [1, 2, 4, 8])
+@pytest.mark.parametrize("kv", [BF16, FP8])
+def test_full_size_h12_131k_sampled(q, kv):
+    prob = inputs.workload_sweep_131k(q, kv_dtype=kv)
     out, lse, _ = run_gpu(prob)
     toks = sorted({0, q - 1})
     o_ref, l_ref = oracle_rows(prob, toks)
