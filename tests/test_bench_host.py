@@ -63,3 +63,23 @@ def test_clock_summary_reads_reasons_and_flags_low_clocks(tmp_path):
     assert s["sm_mhz"] == 1250 and s["sm_max_mhz"] == 2070 and s["samples"] == 3
     assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
     assert s["below_70pct_of_max"] is True
+
+
+def test_oracle_sample_scale_by_hand():
+    # one request, H = 12, ctx 1000, q = 4: the call's rows see 997..1000 keys
+    prob = inputs.make_problem(12, [1000], [4], inputs.KV_BF16, seed=3)
+    whole = (997 + 998 + 999 + 1000) * 12
+    # first token against the whole context: it sees 997 keys
+    sub, scale = bench.oracle_sample(prob, 1)
+    assert list(sub.seq_lens) == [997] and list(sub.q_lens) == [1]
+    assert scale == pytest.approx(whole / (997 * 12))
+    # first two tokens against the first 300 keys: they see 299 and 300
+    sub, scale = bench.oracle_sample(prob, 2, 300)
+    assert list(sub.seq_lens) == [300] and list(sub.q_lens) == [2]
+    assert scale == pytest.approx(whole / ((299 + 300) * 12))
+    # a cap above the context is the whole context; a cap below the token count keeps them
+    assert list(bench.oracle_sample(prob, 1, 10**9)[0].seq_lens) == [997]
+    assert list(bench.oracle_sample(prob, 3, 1)[0].seq_lens) == [3]
+    # the sample's rows are the call's first rows: same query values, same page table row
+    assert (sub.q.float().numpy() == prob.q[:2].float().numpy()).all()
+    assert (sub.page_table[0] == prob.page_table[0]).all()
