@@ -151,17 +151,22 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi sampling (every 20 ms, each sample time-stamped) of the SM clock and the
+    throttle reasons while the bench runs. The summary keeps the samples taken between
+    `begin()` and `end()` (the timed region); when that region is shorter than three
+    sampling periods it also keeps those of the warm-up just before it (same work), and
+    says so."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         import tempfile
 
         self.gpu = gpu_index
         self.proc = None
+        self.t_warm = self.t_begin = self.t_end = None
         fd, self.path = tempfile.mkstemp(prefix=f"mla_bench_clocks_gpu{gpu_index}_", suffix=".csv")
         os.close(fd)
 
@@ -176,12 +181,14 @@ class ClockSampler:
             self.proc = None
         return self
 
-    def mark(self):
-        """Remember where the samples of the timed region begin (the file's current size)."""
-        try:
-            self.start = os.path.getsize(self.path)
-        except OSError:
-            self.start = 0
+    def warmup(self):
+        self.t_warm = time.time()
+
+    def begin(self):
+        self.t_begin = time.time()
+
+    def end(self):
+        self.t_end = time.time()
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -192,25 +199,50 @@ class ClockSampler:
                 self.proc.kill()
             self.fh.close()
 
+    @staticmethod
+    def parse(text: str):
+        """(time in s since the epoch or None, fields after the time stamp) per sample line."""
+        import datetime
+
+        rows = []
+        for line in text.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                t = None
+            rows.append((t, parts[1:]))
+        return rows
+
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as fh:
             text = fh.read()
         try:
             os.remove(self.path)
         except OSError:
             pass
-        lines = text.splitlines()
-        timed = text[getattr(self, "start", 0):].splitlines()
-        if sum(1 for ln in timed if len(ln.split(",")) >= 9) > 0:
-            lines = timed  # samples taken during the timed region only, when there are any
-        for line in lines:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
+        return self.summarize(self.parse(text), self.t_warm, self.t_begin, self.t_end)
+
+    @staticmethod
+    def summarize(rows, t_warm, t_begin, t_end):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        window = "whole run"
+        if t_begin is not None and t_end is not None and all(t is not None for t, _ in rows):
+            timed = [r for r in rows if t_begin <= r[0] <= t_end]
+            window = "timed region"
+            if len(timed) < 3 and t_warm is not None:
+                timed = [r for r in rows if t_warm <= r[0] <= t_end]
+                window = "warm-up + timed region"
+            if timed:
+                rows = timed
+            else:
+                window = "whole run (no sample in the timed region)"
+        sm, smax, reasons = [], [], set()
+        for _, parts in rows:
             try:
                 sm.append(float(parts[1]))
                 smax.append(float(parts[2]))
@@ -223,7 +255,7 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         med = statistics.median(sm)
         return {"sm_mhz": med, "sm_max_mhz": max(smax), "reasons": sorted(reasons), "samples": len(sm),
-                "below_70pct_of_max": med < 0.7 * max(smax)}
+                "window": window, "below_70pct_of_max": med < 0.7 * max(smax)}
 
 
 def run_ours(args, probs, desc, rank, world):
@@ -269,20 +301,22 @@ def run_ours(args, probs, desc, rank, world):
             evs.append((e0, e1))
         return evs
 
-    for _ in range(args.warmup):
-        one_step(False)
-    stream.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
     all_evs = []
     with ClockSampler(dev.index) as clk:
-        clk.mark()
+        clk.warmup()
+        for _ in range(args.warmup):
+            one_step(False)
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        clk.begin()
         t0 = time.perf_counter()
         for _ in range(args.steps):
             all_evs.append(one_step(True))
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - t0
+        clk.end()
     if world > 1:
         torch.distributed.barrier()
     graph_ms = np.array([[e0.elapsed_time(e1) for (e0, e1) in evs] for evs in all_evs])  # [K, calls]

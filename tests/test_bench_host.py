@@ -55,10 +55,10 @@ def test_clock_summary_reads_reasons_and_flags_low_clocks(tmp_path):
     c = bench.ClockSampler(0)
     c.proc = object()  # as if sampling had run
     c.path = str(tmp_path / "clocks.csv")
-    rows = ["0, 1200, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Active",
-            "0, 1300, 2070, 950.0, 0x0, Not Active, Active, Not Active, Not Active",
-            "0, 1250, 2070, 940.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
-    (tmp_path / "clocks.csv").write_text("index, clocks.sm\n" + "\n".join(rows) + "\n")
+    rows = ["2026/12/03 12:00:01.000, 0, 1200, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Active",
+            "2026/12/03 12:00:01.020, 0, 1300, 2070, 950.0, 0x0, Not Active, Active, Not Active, Not Active",
+            "2026/12/03 12:00:01.040, 0, 1250, 2070, 940.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    (tmp_path / "clocks.csv").write_text("timestamp, index, clocks.sm\n" + "\n".join(rows) + "\n")
     s = c.summary()
     assert s["sm_mhz"] == 1250 and s["sm_max_mhz"] == 2070 and s["samples"] == 3
     assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
@@ -83,3 +83,27 @@ def test_oracle_sample_scale_by_hand():
     # the sample's rows are the call's first rows: same query values, same page table row
     assert (sub.q.float().numpy() == prob.q[:2].float().numpy()).all()
     assert (sub.page_table[0] == prob.page_table[0]).all()
+
+
+def test_clock_samples_are_selected_by_time_window():
+    def line(sec, mhz, power_cap="Not Active"):
+        return (f"2026/12/03 12:00:{sec:06.3f}, 0, {mhz}, 2070, 900.5, 0x0000000000000000, Not Active, "
+                f"Not Active, Not Active, {power_cap}")
+
+    text = "\n".join([line(1.0, 1000), line(2.0, 2070), line(2.02, 2070), line(2.04, 2070, "Active"),
+                      line(2.06, 2070), line(3.0, 800), "garbled, line"])
+    rows = bench.ClockSampler.parse(text)
+    assert len(rows) == 6
+    t = [r[0] for r in rows]
+    # the timed region holds four samples: the idle ones before and after are left out
+    s = bench.ClockSampler.summarize(rows, t[0], t[1] - 0.001, t[4] + 0.001)
+    assert s["window"] == "timed region" and s["samples"] == 4
+    assert s["sm_mhz"] == 2070 and s["reasons"] == ["sw_power_cap"]
+    # a timed region with fewer than three samples also takes the warm-up's
+    s = bench.ClockSampler.summarize(rows, t[1] - 0.001, t[3] - 0.001, t[4] + 0.001)
+    assert s["window"] == "warm-up + timed region" and s["samples"] == 4
+    # no window: every sample, and the low median is flagged
+    s = bench.ClockSampler.summarize(rows, None, None, None)
+    assert s["window"] == "whole run" and s["samples"] == 6
+    s = bench.ClockSampler.summarize([rows[0], rows[5]], None, None, None)
+    assert s["below_70pct_of_max"] is True
