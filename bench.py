@@ -416,6 +416,7 @@ def oracle_sample(prob, tokens: int = 1, max_keys: int | None = None):
 
 REF_BUDGET_S = 150.0  # oracle seconds of a whole `--impl reference` run
 CAL_KEYS = 16384  # keys of the calibration sample that sizes each call's timed sample
+_ORACLE_RATE: dict = {}  # call name -> oracle seconds per key of one verify token
 
 
 def cpu_baseline(probs, budget_s: float = 15.0):
@@ -441,8 +442,10 @@ def cpu_baseline(probs, budget_s: float = 15.0):
     us, keys = [], []
     share = budget_s / max(1, len(probs))
     for prob in probs:
-        cal, _ = oracle_sample(prob, 1, CAL_KEYS)
-        rate = timed(cal) / int(cal.seq_lens[0])  # seconds per key of one token
+        rate = _ORACLE_RATE.get(prob.name)
+        if rate is None:  # once per call and process: seconds per key of one token
+            cal, _ = oracle_sample(prob, 1, CAL_KEYS)
+            rate = _ORACLE_RATE[prob.name] = timed(cal) / int(cal.seq_lens[0])
         sub, scale = oracle_sample(prob, 1, max(CAL_KEYS, int(share / max(rate, 1e-12))))
         keys.append(int(sub.seq_lens[0]))
         us.append(timed(sub) * 1e6 * scale)
@@ -467,7 +470,7 @@ def max_over_ranks(x: float, device) -> float:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="sweep")
@@ -495,7 +498,7 @@ def main():
         if rank != 0:
             return
         # each step a bounded sample, sized so that the whole run takes ~REF_BUDGET_S
-        budget = min(30.0, max(2.0, REF_BUDGET_S / (args.warmup + args.steps)))
+        budget = min(30.0, max(1.0, REF_BUDGET_S / (args.warmup + args.steps)))
         times = []
         for i in range(args.warmup + args.steps):
             r = cpu_baseline(probs, budget)
