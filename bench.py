@@ -57,6 +57,13 @@ def workload(name: str):
     if name == "sweep131k":
         return [inputs.workload_sweep_131k(q) for q in (1, 2, 4, 8)], dict(
             workload="h12_ctx131072_bf16_q1-2-4-8", H=12, ctx=131072, q=[1, 2, 4, 8], kv="bf16", page_size=64)
+    if name == "grid":
+        # every cell of a q x ctx x cache-dtype sweep: q 1/2/4/8, ctx 131072 / 524288 / 1048576
+        ctxs = (131072, 1 << 19, 1 << 20)
+        probs = [inputs.workload_sweep_131k(q, ctx=c, kv_dtype=kv) for kv in (inputs.KV_BF16, inputs.KV_FP8)
+                 for c in ctxs for q in (1, 2, 4, 8)]
+        return probs, dict(workload="h12_q1-2-4-8_ctx131072-524288-1048576_bf16+fp8", H=12, ctx=list(ctxs),
+                           q=[1, 2, 4, 8], kv=["bf16", "fp8_e4m3"], page_size=64)
     if name == "sweep131k_fp8":
         return [inputs.workload_sweep_131k(q, kv_dtype=inputs.KV_FP8) for q in (1, 2, 4, 8)], dict(
             workload="h12_ctx131072_fp8_q1-2-4-8", H=12, ctx=131072, q=[1, 2, 4, 8], kv="fp8_e4m3", page_size=64)

@@ -189,6 +189,16 @@ def test_full_size_h12_131k_sampled(q, kv):
     assert_close(out[toks], lse[toks], o_ref, l_ref)
 
 
+@pytest.mark.parametrize("q", [2, 4])
+@pytest.mark.parametrize("kv", [BF16, FP8])
+def test_full_size_h12_512k_sampled(q, kv):
+    prob = inputs.workload_sweep_131k(q, ctx=1 << 19, kv_dtype=kv)
+    out, lse, _ = run_gpu(prob)
+    toks = [0, q - 1]
+    o_ref, l_ref = oracle_rows(prob, toks)
+    assert_close(out[toks], lse[toks], o_ref, l_ref)
+
+
 @pytest.mark.parametrize("kv", [BF16, FP8])
 def test_full_size_h12_1m_sampled(kv):
     prob = inputs.workload_long(kv)
