@@ -299,3 +299,16 @@ def test_long_q_prefill_reduced_ctx(H, q, ctx, kv):
     token with its own causal key range (the earliest of the 2048 sees ctx - 2047 keys),
     whole call against the oracle."""
     _check(inputs.make_problem(H, [ctx], [q], kv, seed=3100 + q, poison_tail=True))
+
+
+@pytest.mark.parametrize("H,kv", [(12, BF16), (12, FP8), (96, BF16)])
+def test_full_size_prefill_sampled(H, kv):
+    """The prefill workload at its full size (q = 2048 tokens against ctx = 131072, the
+    earliest token seeing 129025 keys): sampled tokens at the first, an inner and the last
+    position (inner fold groups and row tiles; for H = 12 token 777 is the second of its
+    8-token fold group), each against the oracle over its causal key prefix."""
+    prob = inputs.make_problem(H, [131072], [2048], kv, seed=1006)
+    out, lse, _ = run_gpu(prob)
+    toks = [0, 777, 2047]
+    o_ref, l_ref = oracle_rows(prob, toks)
+    assert_close(out[toks], lse[toks], o_ref, l_ref)
