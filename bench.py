@@ -73,6 +73,9 @@ def workload(name: str):
     if name == "long_bf16":
         return [inputs.workload_long(inputs.KV_BF16)], dict(workload="h12_q8_ctx1048576_bf16", H=12, ctx=1 << 20, q=[8],
                                                              kv="bf16", page_size=64)
+    if name == "long_bf16_q1":
+        return [inputs.workload_long(inputs.KV_BF16, q=1)], dict(workload="h12_q1_ctx1048576_bf16", H=12,
+                                                                  ctx=1 << 20, q=[1], kv="bf16", page_size=64)
     if name == "long_fp8":
         return [inputs.workload_long(inputs.KV_FP8)], dict(workload="h12_q8_ctx1048576_fp8", H=12, ctx=1 << 20, q=[8],
                                                             kv="fp8_e4m3", page_size=64)
